@@ -1,0 +1,191 @@
+/*
+ * nvfp4.h -- C ABI of the fused NVFP4 linear layer for B300 (sm_103a).
+ *
+ * The operation: a block-scaled 4-bit (NVFP4) GEMM whose trailing small op is applied in
+ * the GEMM epilogue, so each output tile is written to HBM once. Source of the method:
+ * page "How fal made Ideogram V4 6x faster" (news.ditty.ir summary of fal's sub-second
+ * Ideogram V4 post) -- paragraph "first step: run the transformer in NVFP4", the
+ * epilogue-fusion paragraph (RMSNorm with head_dim 256), and the gated-SiLU snippet
+ * "C = A @ B; output = SiLU(C[:, :N//2]) * C[:, N//2:]" with B's columns paired at
+ * weight-packing time.
+ *
+ * NVFP4 tensor format used by every call:
+ *   codes  : uint8 [rows, K/2], row-major, two 4-bit E2M1 codes per byte, element 2j in the
+ *            low nibble of byte j (values +-{0, .5, 1, 1.5, 2, 3, 4, 6}; bit 3 = sign).
+ *   scales : one unsigned E4M3 code per 16 contiguous K-elements of a row, stored in the
+ *            tiled layout the tensor cores read (see nvfp4_scale_offset): tiles of 128 rows
+ *            x 4 blocks = 512 bytes, K-tiles fastest, rows padded to a multiple of 128 with
+ *            zero bytes. Size: nvfp4_scales_bytes(rows, K).
+ *   tensor scale : one fp32 ts = amax(|x|) / (6 * 448); value = e2m1 * e4m3 * ts.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named x, w, codes, scales, bias, gamma, out, workspace, device_error and the
+ *     fp32 tensor-scale pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates, frees or keeps them.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *     and return right after the launch; nothing synchronizes except
+ *     nvfp4_get_device_error.
+ *   - Host-side checks run before anything is launched; a failed check returns a non-zero
+ *     status and launches nothing. A launch failure returns NVFP4_ERR_LAUNCH.
+ *   - Device-side waits are bounded in time. A wait that runs out writes
+ *     NVFP4_ERR_TIMEOUT into *device_error (when device_error is not NULL), frees its
+ *     on-chip resources and ends the kernel; the output is then undefined.
+ *   - Non-finite inputs (inf, NaN) are outside the format; their results are undefined.
+ *   - Requires a compute capability 10.3 GPU (B300); others get NVFP4_ERR_DEVICE.
+ */
+#ifndef NVFP4_H_
+#define NVFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *nvfp4_stream_t;
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_NULL = 1,     /* a required pointer is NULL */
+  NVFP4_ERR_SHAPE = 2,    /* a size or shape rule is broken (see each call) */
+  NVFP4_ERR_ALIGN = 3,    /* a pointer or leading dimension breaks a 16-byte rule */
+  NVFP4_ERR_DEVICE = 4,   /* no current CUDA device, or it is not compute capability 10.3 */
+  NVFP4_ERR_LAUNCH = 5,   /* a CUDA launch or runtime call failed */
+  NVFP4_ERR_TIMEOUT = 6,  /* device-side: a bounded wait ran out (read via device_error) */
+  NVFP4_ERR_ARG = 7       /* an enum or scalar argument is out of range */
+} nvfp4_status;
+
+typedef enum nvfp4_epilogue {
+  NVFP4_EPI_BIAS = 0,          /* y = alpha * acc + bias[n] */
+  NVFP4_EPI_HEAD_RMSNORM = 1,  /* bias, then per-head RMSNorm on columns [0, norm_cols) */
+  NVFP4_EPI_GATED_SILU = 2     /* y[:, j] = SiLU(g_j) * u_j over interleaved (gate, up) pairs */
+} nvfp4_epilogue;
+
+typedef enum nvfp4_out_dtype {
+  NVFP4_OUT_BF16 = 0,  /* round to nearest even */
+  NVFP4_OUT_FP32 = 1
+} nvfp4_out_dtype;
+
+/* Bytes of a tiled scale buffer for `rows` rows of K elements (K % 64 == 0):
+ * ceil(rows / 128) * (K / 64) * 512. Returns 0 for rows <= 0 or a bad K. */
+NVFP4_API size_t nvfp4_scales_bytes(int64_t rows, int64_t K);
+
+/* Byte offset, inside the tiled scale buffer, of the E4M3 scale of row `row` and 16-element
+ * block `kblock` (0 <= kblock < K/16):
+ *   ((row / 128) * (K / 64) + kblock / 4) * 512 + (row % 32) * 16 + ((row / 32) % 4) * 4
+ *   + kblock % 4
+ * This is the 1-D block-scale layout Blackwell tensor cores read (128 rows x 4 scales per
+ * 512-byte tile). Returns -1 for out-of-range arguments. */
+NVFP4_API int64_t nvfp4_scale_offset(int64_t row, int64_t kblock, int64_t K);
+
+/* Bytes of scratch `workspace` that nvfp4_quantize / nvfp4_pack_weights need (16). */
+NVFP4_API size_t nvfp4_workspace_bytes(void);
+
+/*
+ * nvfp4_quantize -- bf16 activations -> NVFP4 (the quantizer that feeds the GEMM).
+ *
+ *   x        bf16 [M, K] with row stride ldx elements (ldx >= K, ldx % 8 == 0, x 16-byte
+ *            aligned).
+ *   codes    out, uint8 [M, K/2] contiguous (16-byte aligned).
+ *   scales   out, nvfp4_scales_bytes(M, K) bytes, tiled layout; padding rows are written 0.
+ *   tensor_scale     out, fp32 [1]: the ts used.
+ *   tensor_scale_in  optional fp32 [1] device pointer. NULL: ts = amax(|x|) / 2688 of this
+ *            x (dynamic per call; costs one extra read of x). Non-NULL: that static ts is
+ *            used and x is read once.
+ *   workspace  >= nvfp4_workspace_bytes() device bytes, 16-byte aligned (amax scratch);
+ *            may be NULL when tensor_scale_in is given.
+ * Per block of 16: s = E4M3(bamax / fp32(6 ts)) (nearest even, saturating at 448);
+ * d = fp32(dec(s) ts); if d < 2^-126 the block stores scale 0 and codes +0; otherwise each
+ * element is coded E2M1(fp32(x * fp32(1/d))) (nearest even, saturating at 6; a negative
+ * value that rounds to 0 keeps its sign, code 0x8). ts <= 0 zeroes everything.
+ * Rules: M >= 0, K > 0, K % 64 == 0, M * K < 2^34. M == 0 launches nothing and returns
+ * NVFP4_OK after the shape checks (the pointers may then be NULL).
+ */
+NVFP4_API nvfp4_status nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx,
+                            uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                            const float *tensor_scale_in, void *workspace,
+                            nvfp4_stream_t stream);
+
+/*
+ * nvfp4_pack_weights -- offline packing of a linear layer's weight W [K, N] (y = x @ W).
+ *
+ *   w        bf16 [K, N] row-major (16-byte aligned, N % 8 == 0).
+ *   gated_interleave  0: packed row n = column n of W.
+ *            1: the gated-SiLU pairing from the page's packing sentence: packed row 2j =
+ *            gate column j, packed row 2j+1 = up column N/2 + j (N even).
+ *   codes    out, uint8 [N, K/2] (K-major: W transposed), 16-byte aligned.
+ *   scales   out, nvfp4_scales_bytes(N, K) bytes, tiled layout.
+ *   tensor_scale  out, fp32 [1]: ts = amax(|W|) / 2688.
+ *   workspace  >= nvfp4_workspace_bytes() device bytes.
+ * Quantization rules are those of nvfp4_quantize, applied to the rows of the packed W^T.
+ * Rules: K > 0, K % 64 == 0, N > 0, N % 8 == 0.
+ */
+NVFP4_API nvfp4_status nvfp4_pack_weights(const void *w, int64_t K, int64_t N, int gated_interleave,
+                                uint8_t *codes, uint8_t *scales, float *tensor_scale,
+                                void *workspace, nvfp4_stream_t stream);
+
+/*
+ * nvfp4_gemm -- block-scaled FP4 GEMM with a fused epilogue.
+ *
+ *   acc[m, n] = sum over 16-blocks kb of sA[m,kb] sB[n,kb] sum_{k in kb} qA[m,k] qB[n,k]
+ *   z[m, n]   = alpha * acc[m, n] + bias[n],   alpha = (*a_ts) * (*b_ts)   (fp32)
+ *
+ *   a_codes/a_scales/a_ts  activations A [M, K] as written by nvfp4_quantize.
+ *   b_codes/b_scales/b_ts  weights B [N, K] (K-major) as written by nvfp4_pack_weights.
+ *   epi  NVFP4_EPI_BIAS:         y = z, out [M, N].
+ *        NVFP4_EPI_HEAD_RMSNORM: columns n < norm_cols, in heads of head_dim columns:
+ *                                y = z * rsqrt(mean_head(z^2) + eps) * gamma[n];
+ *                                other columns y = z. out [M, N].
+ *        NVFP4_EPI_GATED_SILU:   B packed with gated_interleave = 1; for j < N/2,
+ *                                g = z[:, 2j], u = z[:, 2j+1],
+ *                                y[:, j] = g / (1 + exp(-g)) * u. out [M, N/2].
+ *   bias   fp32, NULL for none. Indexed by ORIGINAL output column: length N; for the gated
+ *          epilogue bias[j] belongs to gate column j and bias[N/2 + j] to up column j.
+ *   gamma  fp32 [norm_cols], required for HEAD_RMSNORM, ignored otherwise.
+ *   head_dim  HEAD_RMSNORM: one of 32, 64, 128, 256. norm_cols % head_dim == 0,
+ *          0 <= norm_cols <= N.
+ *   out    16-byte aligned; row stride ldo elements (ldo >= output width; ldo % 8 == 0
+ *          for BF16, % 4 for FP32).
+ *   device_error  optional int [1]: receives NVFP4_ERR_TIMEOUT if a device wait runs out;
+ *          the caller zeroes it. NULL: device timeouts are not reported.
+ * Rules: M >= 0, N > 0, N % 32 == 0, K > 0, K % 64 == 0, all code and scale pointers
+ * 16-byte aligned. M == 0 launches nothing and returns NVFP4_OK after the shape and enum
+ * checks (the pointers may then be NULL).
+ */
+NVFP4_API nvfp4_status nvfp4_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
+                        const uint8_t *b_codes, const uint8_t *b_scales, const float *b_ts,
+                        int64_t M, int64_t N, int64_t K, nvfp4_epilogue epi,
+                        const float *bias, const float *gamma, int head_dim,
+                        int64_t norm_cols, float eps, nvfp4_out_dtype out_dtype, void *out,
+                        int64_t ldo, int *device_error, nvfp4_stream_t stream);
+
+/* Synchronizes `stream`, copies *device_error to *code, then zeroes the device word.
+ * Returns NVFP4_ERR_NULL for NULL pointers, NVFP4_ERR_LAUNCH if a CUDA call fails. */
+NVFP4_API nvfp4_status nvfp4_get_device_error(int *device_error, int *code, nvfp4_stream_t stream);
+
+/* Static, human-readable name of a status code ("NVFP4_OK", ...). Never NULL. */
+NVFP4_API const char *nvfp4_status_string(nvfp4_status status);
+
+/*
+ * nvfp4_debug_wait_timeout -- exercises the bounded device wait.
+ * Launches one small kernel that waits on an on-chip barrier that nothing ever completes,
+ * for at most timeout_ns nanoseconds (1 <= timeout_ns <= 10^10), then writes
+ * NVFP4_ERR_TIMEOUT into *device_error and returns normally; the CUDA context stays usable.
+ * Used by the tests of the error path; it computes nothing.
+ */
+NVFP4_API nvfp4_status nvfp4_debug_wait_timeout(int *device_error, int64_t timeout_ns,
+                                      nvfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H_ */

@@ -1,0 +1,171 @@
+"""Python binding of libnvfp4.so, the fused NVFP4 linear layer for B300 (sm_103a).
+
+Argument marshalling only: torch tensors supply device memory and the current CUDA stream,
+and every step of the path runs in the library's CUDA kernels. There is no CPU fallback:
+if the library is missing or the device is not a B300, calls raise.
+
+    from nvfp4_gemm_act_b300 import nvfp4_quantize, nvfp4_pack_weights, nvfp4_gemm
+    a = nvfp4_quantize(x)                                   # x: bf16 [M, K] on cuda
+    b = nvfp4_pack_weights(w, gated_interleave=True)        # w: bf16 [K, N] on cuda
+    y = nvfp4_gemm(a, b, "gated_silu")                      # bf16 [M, N/2]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
+
+EPILOGUES = {"bias": 0, "head_rmsnorm": 1, "gated_silu": 2}
+OUT_DTYPES = {torch.bfloat16: 0, torch.float32: 1}
+STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_NULL", 2: "NVFP4_ERR_SHAPE", 3: "NVFP4_ERR_ALIGN",
+          4: "NVFP4_ERR_DEVICE", 5: "NVFP4_ERR_LAUNCH", 6: "NVFP4_ERR_TIMEOUT", 7: "NVFP4_ERR_ARG"}
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SIGS = {
+    "nvfp4_scales_bytes": (ctypes.c_size_t, [_I64, _I64]),
+    "nvfp4_scale_offset": (_I64, [_I64, _I64, _I64]),
+    "nvfp4_workspace_bytes": (ctypes.c_size_t, []),
+    "nvfp4_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P]),
+    "nvfp4_pack_weights": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_int, _P, _P, _P, _P, _P]),
+    "nvfp4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P,
+                                  ctypes.c_int, _I64, ctypes.c_float, ctypes.c_int, _P, _I64, _P, _P]),
+    "nvfp4_get_device_error": (ctypes.c_int, [_P, _P, _P]),
+    "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "nvfp4_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
+}
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, func: str, status: int):
+        super().__init__(f"{func} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C-ABI library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing; build it with "
+                               "`python -m nvfp4_gemm_act_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(func: str, status: int) -> None:
+    if status != 0:
+        raise Nvfp4Error(func, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+class Nvfp4Tensor(NamedTuple):
+    """A row-major NVFP4 matrix: codes uint8 [rows, K/2], tiled E4M3 scales, fp32 ts [1]."""
+    codes: torch.Tensor
+    scales: torch.Tensor
+    ts: torch.Tensor
+    rows: int
+    K: int
+
+
+def nvfp4_scales_bytes(rows: int, K: int) -> int:
+    return lib().nvfp4_scales_bytes(rows, K)
+
+
+def nvfp4_scale_offset(row: int, kblock: int, K: int) -> int:
+    return lib().nvfp4_scale_offset(row, kblock, K)
+
+
+def nvfp4_workspace_bytes() -> int:
+    return lib().nvfp4_workspace_bytes()
+
+
+def _alloc_nvfp4(rows: int, K: int, device) -> Nvfp4Tensor:
+    codes = torch.empty((rows, K // 2), dtype=torch.uint8, device=device)
+    scales = torch.empty(max(nvfp4_scales_bytes(rows, K), 16), dtype=torch.uint8, device=device)
+    ts = torch.empty(1, dtype=torch.float32, device=device)
+    return Nvfp4Tensor(codes, scales, ts, rows, K)
+
+
+def nvfp4_quantize(x: torch.Tensor, tensor_scale_in: Optional[torch.Tensor] = None,
+                   out: Optional[Nvfp4Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                   stream=None) -> Nvfp4Tensor:
+    """bf16 [M, K] (row stride x.stride(0)) -> Nvfp4Tensor, via nvfp4_quantize."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        out = _alloc_nvfp4(M, K, x.device)
+    if workspace is None and tensor_scale_in is None:
+        workspace = torch.empty(nvfp4_workspace_bytes(), dtype=torch.uint8, device=x.device)
+    _check("nvfp4_quantize", lib().nvfp4_quantize(
+        _ptr(x), M, K, x.stride(0), _ptr(out.codes), _ptr(out.scales), _ptr(out.ts),
+        _ptr(tensor_scale_in), _ptr(workspace), _stream(stream)))
+    return out
+
+
+def nvfp4_pack_weights(w: torch.Tensor, gated_interleave: bool = False,
+                       out: Optional[Nvfp4Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                       stream=None) -> Nvfp4Tensor:
+    """bf16 W [K, N] -> K-major Nvfp4Tensor [N, K] (gated pair interleave optional)."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.is_contiguous()
+    K, N = w.shape
+    if out is None:
+        out = _alloc_nvfp4(N, K, w.device)
+    if workspace is None:
+        workspace = torch.empty(nvfp4_workspace_bytes(), dtype=torch.uint8, device=w.device)
+    _check("nvfp4_pack_weights", lib().nvfp4_pack_weights(
+        _ptr(w), K, N, int(bool(gated_interleave)), _ptr(out.codes), _ptr(out.scales),
+        _ptr(out.ts), _ptr(workspace), _stream(stream)))
+    return out
+
+
+def nvfp4_gemm(a: Nvfp4Tensor, b: Nvfp4Tensor, epilogue: str = "bias",
+               bias: Optional[torch.Tensor] = None, gamma: Optional[torch.Tensor] = None,
+               head_dim: int = 256, norm_cols: int = 0, eps: float = 1e-6,
+               out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+               device_error: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Fused NVFP4 GEMM: epilogue(alpha * A B^T + bias) -> out [M, N] (gated: [M, N/2])."""
+    assert a.K == b.K
+    M, N, K = a.rows, b.rows, a.K
+    width = N // 2 if epilogue == "gated_silu" else N
+    if out is None:
+        out = torch.empty((M, width), dtype=out_dtype, device=a.codes.device)
+    assert out.dtype == out_dtype and out.stride(1) == 1
+    _check("nvfp4_gemm", lib().nvfp4_gemm(
+        _ptr(a.codes), _ptr(a.scales), _ptr(a.ts), _ptr(b.codes), _ptr(b.scales), _ptr(b.ts),
+        M, N, K, EPILOGUES[epilogue], _ptr(bias), _ptr(gamma), head_dim, norm_cols, eps,
+        OUT_DTYPES[out_dtype], _ptr(out), out.stride(0), _ptr(device_error), _stream(stream)))
+    return out
+
+
+def nvfp4_get_device_error(device_error: torch.Tensor, stream=None) -> int:
+    """Synchronizes the stream, returns the device error word and clears it."""
+    code = ctypes.c_int(0)
+    _check("nvfp4_get_device_error", lib().nvfp4_get_device_error(
+        _ptr(device_error), ctypes.addressof(code), _stream(stream)))
+    return code.value
+
+
+def nvfp4_debug_wait_timeout(device_error: torch.Tensor, timeout_ns: int, stream=None) -> None:
+    _check("nvfp4_debug_wait_timeout", lib().nvfp4_debug_wait_timeout(
+        _ptr(device_error), timeout_ns, _stream(stream)))

@@ -1,0 +1,219 @@
+// C ABI of the fused NVFP4 linear layer (declared in include/nvfp4.h): argument checks,
+// device check, and dispatch to the kernels. Every check runs before anything is launched.
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/nvfp4.h"
+#include "nvfp4_internal.h"
+
+namespace nvfp4 {
+
+uint64_t wait_timeout_ns() {
+  static const uint64_t v = [] {
+    const char* s = std::getenv("NVFP4_WAIT_TIMEOUT_NS");
+    if (s != nullptr) {
+      const unsigned long long t = std::strtoull(s, nullptr, 10);
+      if (t > 0) return static_cast<uint64_t>(t);
+    }
+    return static_cast<uint64_t>(2000000000ull);
+  }();
+  return v;
+}
+
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  int v = cached[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    cached[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+int resident_blocks(const void* kernel, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n <= 0) n = 1;
+  return n;
+}
+
+}  // namespace nvfp4
+
+namespace {
+
+constexpr int64_t kMaxElems = int64_t(1) << 34;  // M * K bound of the 32-bit work indices
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device must be compute capability 10.3 (B300). Cached per device.
+nvfp4_status check_device() {
+  static std::atomic<int> state[64];  // 0 unknown, 1 ok, 2 bad
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    (void)cudaGetLastError();
+    return NVFP4_ERR_DEVICE;
+  }
+  if (dev < 64) {
+    const int st = state[dev].load(std::memory_order_relaxed);
+    if (st == 1) return NVFP4_OK;
+    if (st == 2) return NVFP4_ERR_DEVICE;
+  }
+  int major = 0, minor = 0;
+  bool ok = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess &&
+            major == 10 && minor == 3;
+  if (!ok) (void)cudaGetLastError();
+  if (dev < 64) state[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
+  return ok ? NVFP4_OK : NVFP4_ERR_DEVICE;
+}
+
+nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH; }
+
+}  // namespace
+
+extern "C" {
+
+size_t nvfp4_scales_bytes(int64_t rows, int64_t K) {
+  if (rows <= 0 || K <= 0 || K % 64 != 0) return 0;
+  return static_cast<size_t>((rows + 127) / 128) * static_cast<size_t>(K / 64) * 512u;
+}
+
+int64_t nvfp4_scale_offset(int64_t row, int64_t kblock, int64_t K) {
+  if (row < 0 || kblock < 0 || K <= 0 || K % 64 != 0 || kblock >= K / 16) return -1;
+  return ((row / 128) * (K / 64) + kblock / 4) * 512 + (row % 32) * 16 + ((row / 32) % 4) * 4 + kblock % 4;
+}
+
+size_t nvfp4_workspace_bytes(void) { return 16; }
+
+const char* nvfp4_status_string(nvfp4_status s) {
+  switch (s) {
+    case NVFP4_OK: return "NVFP4_OK";
+    case NVFP4_ERR_NULL: return "NVFP4_ERR_NULL";
+    case NVFP4_ERR_SHAPE: return "NVFP4_ERR_SHAPE";
+    case NVFP4_ERR_ALIGN: return "NVFP4_ERR_ALIGN";
+    case NVFP4_ERR_DEVICE: return "NVFP4_ERR_DEVICE";
+    case NVFP4_ERR_LAUNCH: return "NVFP4_ERR_LAUNCH";
+    case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+    case NVFP4_ERR_ARG: return "NVFP4_ERR_ARG";
+  }
+  return "NVFP4_ERR_UNKNOWN";
+}
+
+nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                            uint8_t* scales, float* tensor_scale, const float* tensor_scale_in,
+                            void* workspace, nvfp4_stream_t stream) {
+  if (M < 0 || K <= 0 || K % 64 != 0 || ldx < K) return NVFP4_ERR_SHAPE;
+  if (M > 0 && K > kMaxElems / M) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;  // empty: nothing is read or written (pointers may be NULL)
+  if (x == nullptr || codes == nullptr || scales == nullptr || tensor_scale == nullptr)
+    return NVFP4_ERR_NULL;
+  if (tensor_scale_in == nullptr && workspace == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(x) || ldx % 8 != 0 || !aligned16(codes) || !aligned16(scales) ||
+      (workspace != nullptr && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
+    return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned* amax = static_cast<unsigned*>(workspace);
+  if (tensor_scale_in == nullptr) {
+    if (cudaMemsetAsync(amax, 0, sizeof(unsigned), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+    if (nvfp4_status st = from_cuda(nvfp4::launch_amax(x, M, K, ldx, amax, s)); st != NVFP4_OK) return st;
+  }
+  return from_cuda(nvfp4::launch_quantize(x, M, K, ldx, codes, scales, amax, tensor_scale_in, tensor_scale, s));
+}
+
+nvfp4_status nvfp4_pack_weights(const void* w, int64_t K, int64_t N, int gated_interleave, uint8_t* codes,
+                                uint8_t* scales, float* tensor_scale, void* workspace, nvfp4_stream_t stream) {
+  if (w == nullptr || codes == nullptr || scales == nullptr || tensor_scale == nullptr || workspace == nullptr)
+    return NVFP4_ERR_NULL;
+  if (gated_interleave != 0 && gated_interleave != 1) return NVFP4_ERR_ARG;
+  if (K <= 0 || K % 64 != 0 || N <= 0 || N % 8 != 0) return NVFP4_ERR_SHAPE;
+  if (K > kMaxElems / N || K / 64 > 65535) return NVFP4_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(codes) || !aligned16(scales) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
+    return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned* amax = static_cast<unsigned*>(workspace);
+  if (cudaMemsetAsync(amax, 0, sizeof(unsigned), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  if (cudaMemsetAsync(scales, 0, nvfp4_scales_bytes(N, K), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  if (nvfp4_status st = from_cuda(nvfp4::launch_amax(w, K, N, N, amax, s)); st != NVFP4_OK) return st;
+  return from_cuda(nvfp4::launch_pack_weights(w, K, N, gated_interleave == 1, codes, scales, amax, tensor_scale, s));
+}
+
+nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_ts,
+                        const uint8_t* b_codes, const uint8_t* b_scales, const float* b_ts, int64_t M,
+                        int64_t N, int64_t K, nvfp4_epilogue epi, const float* bias, const float* gamma,
+                        int head_dim, int64_t norm_cols, float eps, nvfp4_out_dtype out_dtype, void* out,
+                        int64_t ldo, int* device_error, nvfp4_stream_t stream) {
+  if (epi != NVFP4_EPI_BIAS && epi != NVFP4_EPI_HEAD_RMSNORM && epi != NVFP4_EPI_GATED_SILU)
+    return NVFP4_ERR_ARG;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_ARG;
+  if (epi == NVFP4_EPI_HEAD_RMSNORM) {
+    if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256) return NVFP4_ERR_ARG;
+    if (!(eps >= 0.0f) || eps != eps) return NVFP4_ERR_ARG;
+  }
+  if (M < 0 || N <= 0 || N % 32 != 0 || K <= 0 || K % 64 != 0) return NVFP4_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
+  if (epi == NVFP4_EPI_HEAD_RMSNORM && (norm_cols < 0 || norm_cols > N || norm_cols % head_dim != 0))
+    return NVFP4_ERR_SHAPE;
+  const int64_t out_cols = epi == NVFP4_EPI_GATED_SILU ? N / 2 : N;
+  if (ldo < out_cols) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;  // empty: nothing is read or written (pointers may be NULL)
+  if (a_codes == nullptr || a_scales == nullptr || a_ts == nullptr || b_codes == nullptr ||
+      b_scales == nullptr || b_ts == nullptr || out == nullptr)
+    return NVFP4_ERR_NULL;
+  if (epi == NVFP4_EPI_HEAD_RMSNORM && gamma == nullptr && norm_cols > 0) return NVFP4_ERR_NULL;
+  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(b_codes) || !aligned16(b_scales) ||
+      !aligned16(out) || ldo % (out_dtype == NVFP4_OUT_BF16 ? 8 : 4) != 0)
+    return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  nvfp4::GemmArgs a;
+  a.a_codes = a_codes;
+  a.a_scales = a_scales;
+  a.a_ts = a_ts;
+  a.b_codes = b_codes;
+  a.b_scales = b_scales;
+  a.b_ts = b_ts;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.epi = static_cast<int>(epi);
+  a.bias = bias;
+  a.gamma = gamma;
+  a.head_dim = epi == NVFP4_EPI_HEAD_RMSNORM ? head_dim : 256;
+  a.norm_cols = epi == NVFP4_EPI_HEAD_RMSNORM ? norm_cols : 0;
+  a.eps = eps;
+  a.out_fp32 = out_dtype == NVFP4_OUT_FP32 ? 1 : 0;
+  a.out = out;
+  a.ldo = ldo;
+  a.err = device_error;
+  return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_get_device_error(int* device_error, int* code, nvfp4_stream_t stream) {
+  if (device_error == nullptr || code == nullptr) return NVFP4_ERR_NULL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, device_error, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return NVFP4_ERR_LAUNCH;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  *code = host;
+  if (cudaMemsetAsync(device_error, 0, sizeof(int), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_debug_wait_timeout(int* device_error, int64_t timeout_ns, nvfp4_stream_t stream) {
+  if (device_error == nullptr) return NVFP4_ERR_NULL;
+  if (timeout_ns < 1 || timeout_ns > 10000000000ll) return NVFP4_ERR_ARG;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  return from_cuda(nvfp4::launch_wait_timeout(device_error, static_cast<uint64_t>(timeout_ns),
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

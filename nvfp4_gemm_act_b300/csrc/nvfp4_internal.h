@@ -1,0 +1,58 @@
+// Internal host-side interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+// Default bound on any single device-side wait (2 s); NVFP4_WAIT_TIMEOUT_NS overrides it.
+uint64_t wait_timeout_ns();
+
+// Blocks per SM the kernel can keep resident with `threads` threads and `smem` dynamic bytes.
+int resident_blocks(const void* kernel, int threads, size_t smem);
+int sm_count();
+
+// amax(|x|) of bf16 x [rows, cols] (row stride ld) into *amax_bits (fp32 bit pattern,
+// atomic max; the caller zeroes it first).
+cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                        unsigned* amax_bits, cudaStream_t s);
+
+// Quantize x [M, K] (row stride ldx). ts = *ts_in if ts_in, else amax/2688 from *amax_bits.
+cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
+                            uint8_t* scales, const unsigned* amax_bits, const float* ts_in,
+                            float* ts_out, cudaStream_t s);
+
+// W [K, N] -> packed K-major codes [N, K/2] + tiled scales (scales pre-zeroed by caller).
+cudaError_t launch_pack_weights(const void* w, int64_t K, int64_t N, bool gated,
+                                uint8_t* codes, uint8_t* scales, const unsigned* amax_bits,
+                                float* ts_out, cudaStream_t s);
+
+struct GemmArgs {
+  const uint8_t* a_codes;
+  const uint8_t* a_scales;
+  const float* a_ts;
+  const uint8_t* b_codes;
+  const uint8_t* b_scales;
+  const float* b_ts;
+  int64_t M, N, K;
+  int epi;
+  const float* bias;
+  const float* gamma;
+  int head_dim;
+  int64_t norm_cols;
+  float eps;
+  int out_fp32;
+  void* out;
+  int64_t ldo;
+  int* err;
+};
+
+// Validated arguments in, kernel launched (or an error code out).
+nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s);
+
+cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace nvfp4

@@ -1,0 +1,136 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_gemm_act_b300 as nv
+from oracle import nvfp4_ref as R
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4.h")
+
+pytestmark = pytest.mark.skipif(not os.path.exists(nv.LIB_PATH), reason="libnvfp4.so not built")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DEVICE, ERR_ARG = 0, 1, 2, 3, 4, 7
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: every call below fails a host check
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_\w+)\s*\(", text)))
+
+
+def test_header_symbols_are_exported():
+    names = header_functions()
+    assert {"nvfp4_quantize", "nvfp4_pack_weights", "nvfp4_gemm"} <= set(names)
+    L = ctypes.CDLL(nv.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    # and every exported entry point has a Python binding with the same name
+    for n in names:
+        assert n in nv._SIGS, n
+
+
+def test_only_header_symbols_are_exported():
+    out = os.popen(f"nm -D --defined-only {nv.LIB_PATH}").read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    ours = {s for s in exported if s.startswith("nvfp4")}
+    assert ours == set(header_functions())
+
+
+def test_status_strings():
+    for code, name in nv.STATUS.items():
+        assert nv.lib().nvfp4_status_string(code).decode() == name
+    assert nv.lib().nvfp4_status_string(99).decode() == "NVFP4_ERR_UNKNOWN"
+
+
+def test_scale_helpers_match_the_oracle_layout():
+    for rows, K in [(1, 64), (128, 256), (200, 3072), (4608, 12288)]:
+        assert nv.nvfp4_scales_bytes(rows, K) == R.scales_bytes(rows, K)
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        K = int(rng.integers(1, 200)) * 64
+        r, kb = int(rng.integers(0, 5000)), int(rng.integers(0, K // 16))
+        assert nv.nvfp4_scale_offset(r, kb, K) == int(R.scale_offset(r, kb, K))
+    assert nv.nvfp4_scale_offset(0, 4, 64) == -1 and nv.nvfp4_scale_offset(-1, 0, 64) == -1
+    assert nv.nvfp4_scales_bytes(0, 64) == 0 and nv.nvfp4_scales_bytes(4, 96) == 0
+    assert nv.nvfp4_workspace_bytes() == 16
+
+
+def q(x=FAKE, M=128, K=256, ldx=256, codes=FAKE, scales=FAKE, ts=FAKE, ts_in=None, ws=FAKE):
+    return nv.lib().nvfp4_quantize(x, M, K, ldx, codes, scales, ts, ts_in, ws, None)
+
+
+def test_quantize_host_checks():
+    assert q(x=None) == ERR_NULL
+    assert q(codes=None) == ERR_NULL
+    assert q(ws=None) == ERR_NULL                  # dynamic scale needs the workspace
+    assert q(K=96, ldx=96) == ERR_SHAPE            # K % 64
+    assert q(K=0, ldx=0) == ERR_SHAPE
+    assert q(M=-1) == ERR_SHAPE
+    assert q(ldx=128) == ERR_SHAPE                 # ldx < K
+    assert q(M=1 << 22, K=1 << 13, ldx=1 << 13) == ERR_SHAPE  # beyond 2^34 elements
+    assert q(x=FAKE + 8) == ERR_ALIGN
+    assert q(ldx=260) == ERR_ALIGN
+    assert q(codes=FAKE + 4) == ERR_ALIGN
+    assert q(M=0) == OK                            # empty: nothing launched
+    assert q(M=0, x=None, codes=None) == OK        # empty tensors may have NULL storage
+
+
+def g(**kw):
+    a = dict(ac=FAKE, asc=FAKE, ats=FAKE, bc=FAKE, bsc=FAKE, bts=FAKE, M=128, N=256, K=256, epi=0,
+             bias=None, gamma=None, hd=256, nc=0, eps=1e-6, od=0, out=FAKE, ldo=256, err=None)
+    a.update(kw)
+    return nv.lib().nvfp4_gemm(a["ac"], a["asc"], a["ats"], a["bc"], a["bsc"], a["bts"], a["M"], a["N"],
+                               a["K"], a["epi"], a["bias"], a["gamma"], a["hd"], a["nc"], a["eps"],
+                               a["od"], a["out"], a["ldo"], a["err"], None)
+
+
+def test_gemm_host_checks():
+    assert g(ac=None) == ERR_NULL
+    assert g(out=None) == ERR_NULL
+    assert g(epi=1, nc=256, gamma=None) == ERR_NULL
+    assert g(epi=5) == ERR_ARG
+    assert g(od=3) == ERR_ARG
+    assert g(epi=1, hd=96, gamma=FAKE, nc=192) == ERR_ARG
+    assert g(epi=1, gamma=FAKE, nc=256, eps=-1.0) == ERR_ARG
+    assert g(K=96) == ERR_SHAPE
+    assert g(N=48, ldo=48) == ERR_SHAPE            # N % 32
+    assert g(epi=1, gamma=FAKE, nc=128) == ERR_SHAPE   # norm_cols % head_dim
+    assert g(epi=1, gamma=FAKE, nc=512) == ERR_SHAPE   # norm_cols > N
+    assert g(ldo=128) == ERR_SHAPE
+    assert g(epi=2, ldo=128) != ERR_SHAPE          # gated output is N/2 wide
+    assert g(ac=FAKE + 1) == ERR_ALIGN
+    assert g(ldo=260) == ERR_ALIGN
+    assert g(od=1, ldo=260) == ERR_SHAPE or g(od=1, ldo=260) != ERR_ALIGN
+    assert g(M=0) == OK
+    assert g(M=0, ac=None) == OK
+
+
+def test_pack_host_checks():
+    L = nv.lib()
+    assert L.nvfp4_pack_weights(None, 256, 256, 0, FAKE, FAKE, FAKE, FAKE, None) == ERR_NULL
+    assert L.nvfp4_pack_weights(FAKE, 256, 256, 2, FAKE, FAKE, FAKE, FAKE, None) == ERR_ARG
+    assert L.nvfp4_pack_weights(FAKE, 100, 256, 0, FAKE, FAKE, FAKE, FAKE, None) == ERR_SHAPE
+    assert L.nvfp4_pack_weights(FAKE, 256, 12, 0, FAKE, FAKE, FAKE, FAKE, None) == ERR_SHAPE
+    assert L.nvfp4_pack_weights(FAKE + 2, 256, 256, 0, FAKE, FAKE, FAKE, FAKE, None) == ERR_ALIGN
+
+
+def test_debug_timeout_host_checks():
+    L = nv.lib()
+    assert L.nvfp4_debug_wait_timeout(None, 1000, None) == ERR_NULL
+    assert L.nvfp4_debug_wait_timeout(FAKE, 0, None) == ERR_ARG
+    assert L.nvfp4_get_device_error(None, None, None) == ERR_NULL
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_valid_arguments_without_a_gpu_report_the_device():
+    assert q() == ERR_DEVICE
+    assert g() == ERR_DEVICE
+    assert nv.lib().nvfp4_debug_wait_timeout(FAKE, 1000, None) == ERR_DEVICE

@@ -1,0 +1,142 @@
+"""GPU parity of the quantizer and the weight packer against the oracle: bit-exact codes,
+scales and tensor scales (calls go through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import nvfp4_gemm_act_b300 as nv
+from nvfp4_gemm_act_b300 import workloads as W
+from oracle import nvfp4_ref as R
+
+from parity import assert_quant_equal, gpu_nvfp4_to_np, to_np_f32
+from test_oracle_quantize import _load_quant_golden
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
+
+
+def quant_both(x_bf16: torch.Tensor, ts_in=None, what=""):
+    tsi = None if ts_in is None else torch.tensor([ts_in], dtype=torch.float32, device=DEV)
+    q = nv.nvfp4_quantize(x_bf16.to(DEV), tensor_scale_in=tsi)
+    gpu = gpu_nvfp4_to_np(q)
+    ref = R.quantize_ref(to_np_f32(x_bf16), ts_in)
+    assert_quant_equal(gpu, ref, what)
+    return q
+
+
+def test_hand_worked_fixture_on_gpu():
+    x, s, qc, ts = _load_quant_golden()
+    q = nv.nvfp4_quantize(_bf16(x).to(DEV))
+    gc, gs, gt = gpu_nvfp4_to_np(q)
+    assert gt == np.float32(ts)
+    assert np.array_equal(gs, s)
+    assert np.array_equal(gc, qc)
+
+
+def test_tiny_activations():
+    quant_both(W.make_x(W.TINY_BIAS), what="tiny")
+
+
+@pytest.mark.parametrize("M", [1, 127, 129, 200])
+def test_ragged_rows_and_zero_padding(M):
+    x = W.make_x(W.QKV_RMSNORM.with_m(M))
+    q = quant_both(x, what=f"M={M}")
+    buf = q.scales.cpu().numpy()
+    used = np.zeros(buf.size, bool)
+    r, kb = np.meshgrid(np.arange(M), np.arange(x.shape[1] // 16), indexing="ij")
+    used[R.scale_offset(r, kb, x.shape[1])] = True
+    assert not buf[~used].any(), "padding rows of the scale tiles must be zero"
+
+
+def test_qkv_activations_full_size():
+    quant_both(W.make_x(W.QKV_RMSNORM), what="qkv X 4608x3072")
+
+
+def test_down_activations_full_size_sampled_rows():
+    w = W.DOWN_BIAS
+    x = W.make_x(w)
+    q = nv.nvfp4_quantize(x.to(DEV))
+    gc, gs, gt = gpu_nvfp4_to_np(q)
+    xn = to_np_f32(x)
+    ts = R.tensor_scale_ref(xn)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 4607],
+                                     np.random.default_rng(7).integers(0, w.M, 58)]))
+    rc, rs, _ = R.quantize_ref(xn[rows], ts)
+    assert_quant_equal((gc[rows], gs[rows], gt), (rc, rs, ts), "down X sampled")
+
+
+def test_static_tensor_scale():
+    x = W.make_x(W.TINY_BIAS)
+    quant_both(x, ts_in=np.float32(1e-3), what="static small ts (saturating)")
+    quant_both(x, ts_in=np.float32(0.05), what="static large ts")
+
+
+def test_zero_tensor_and_degenerate_values():
+    quant_both(torch.zeros(64, 128, dtype=torch.bfloat16), what="zeros")
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((64, 256))
+    x[:, :16] *= 1e-30                  # blocks far below the tensor amax: E4M3 underflow
+    x[1] = -0.0                          # negative zeros
+    x[2, ::3] = 0.0
+    x[3] *= 1e-35                        # tiny row, still live blocks
+    quant_both(_bf16(x), what="degenerate")
+    t = np.full((8, 64), 1e-38)          # tiny tensor: fp32 subnormal products
+    t[0, 0] = 3e-38
+    quant_both(_bf16(t), what="tiny tensor")
+
+
+def test_strided_rows():
+    x = W.make_x(W.QKV_RMSNORM.with_m(96))
+    big = torch.zeros(96, 3072 + 64, dtype=torch.bfloat16)
+    big[:, :3072] = x
+    view = big.to(DEV)[:, :3072]
+    assert view.stride(0) == 3136
+    q = nv.nvfp4_quantize(view)
+    assert_quant_equal(gpu_nvfp4_to_np(q), R.quantize_ref(to_np_f32(x)), "strided")
+
+
+def test_empty_input_is_a_no_op():
+    x = torch.zeros(0, 256, dtype=torch.bfloat16, device=DEV)
+    q = nv.nvfp4_quantize(x)
+    torch.cuda.synchronize()
+    assert q.codes.numel() == 0
+
+
+def pack_both(w_bf16, gated, what):
+    q = nv.nvfp4_pack_weights(w_bf16.to(DEV), gated_interleave=gated)
+    gpu = gpu_nvfp4_to_np(q)
+    ref = R.pack_weights_ref(to_np_f32(w_bf16), gated)
+    assert_quant_equal(gpu, ref, what)
+    return q
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_pack_small(gated):
+    pack_both(W.make_w(W.TINY_BIAS), gated, f"tiny W gated={gated}")
+
+
+@pytest.mark.parametrize("K,N", [(64, 8), (128, 72), (320, 200)])
+def test_pack_ragged(K, N):
+    rng = np.random.default_rng(K + N)
+    w = _bf16(rng.standard_normal((K, N)) * 0.02)
+    pack_both(w, False, f"W {K}x{N}")
+    if N % 2 == 0:
+        pack_both(w, True, f"W {K}x{N} gated")
+
+
+def test_pack_gated_up_full_size_sampled_rows():
+    w = W.GATED_UP
+    wt = W.make_w(w)
+    q = nv.nvfp4_pack_weights(wt.to(DEV), gated_interleave=True)
+    gc, gs, gt = gpu_nvfp4_to_np(q)
+    wn = to_np_f32(wt)
+    ts = R.tensor_scale_ref(wn)
+    perm = R.gated_permutation(w.N)
+    rows = np.unique(np.concatenate([[0, 1, 2, 3, w.N - 2, w.N - 1, 12287, 12288],
+                                     np.random.default_rng(8).integers(0, w.N, 56)]))
+    rc, rs, _ = R.quantize_ref(np.ascontiguousarray(wn.T[perm[rows]]), ts)
+    assert_quant_equal((gc[rows], gs[rows], gt), (rc, rs, ts), "gated W sampled")
