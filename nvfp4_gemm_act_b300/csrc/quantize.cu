@@ -71,12 +71,6 @@ __device__ __forceinline__ uint32_t encode8(const uint4& v, float inv) {
   return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
 }
 
-// Byte offset of the 4-byte scale word of (row, 64-element group g) in the tiled layout:
-// tiles of 128 rows x 4 blocks (512 B), K-tiles fastest; row r at line r%32, slot (r/32)%4.
-__device__ __forceinline__ uint32_t scale_word_offset(uint32_t row, uint32_t g, uint32_t gpr) {
-  return ((row >> 7) * gpr + g) * 512u + (row & 31u) * 16u + ((row >> 5) & 3u) * 4u;
-}
-
 // ---------------------------------------------------------------------------------------
 // amax: 128-bit loads, packed 16-bit max, warp reduce, one atomicMax per block.
 // ---------------------------------------------------------------------------------------
@@ -128,62 +122,64 @@ __global__ void __launch_bounds__(kAmaxThreads)
 }
 
 // ---------------------------------------------------------------------------------------
-// Activation quantizer. A warp covers 4 groups of 64 elements per step (lane = 8 elements,
-// a lane pair = one 16-element block, 8 lanes = one group = one 4-byte scale word); every
-// load instruction reads 512 contiguous bytes of a row. kQuantUnroll steps are in flight.
-// Rows in [M, Mpad) only write their (zero) scale words.
+// Activation quantizer. Work item = one 512-element chunk of a row; lane l owns the
+// 16-element block c * 32 + l (two 16-byte loads), so a warp reads 1 KB of a row per item
+// and writes 256 contiguous code bytes. Items are visited in reverse order (a grid-stride
+// walk from the end of x), so the data the amax pass read last -- still in L2 -- is
+// quantized first. Rows in [M, Mpad) only write their zero scale bytes.
 // ---------------------------------------------------------------------------------------
 constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;
 
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M,
-                    uint32_t gpr, uint32_t total_groups, uint8_t* __restrict__ codes,
-                    uint8_t* __restrict__ scales, const unsigned* __restrict__ amax_bits,
-                    const float* __restrict__ ts_in, float* __restrict__ ts_out) {
+                    uint32_t blocks_per_row, uint32_t chunks_per_row, uint32_t total_items,
+                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                    const unsigned* __restrict__ amax_bits, const float* __restrict__ ts_in,
+                    float* __restrict__ ts_out) {
   const float ts = ts_in != nullptr ? *ts_in : __fdiv_rn(__uint_as_float(*amax_bits), kTsDivisor);
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
   const float six_ts = __fmul_rn(6.0f, ts);
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t sub = lane & 7u;
-  const uint32_t grp_lane0 = lane & ~7u;
   const uint32_t warp = (blockIdx.x * kQuantThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kQuantThreads) >> 5;
-  const uint64_t row_code_bytes = (uint64_t)gpr * 32u;
+  const uint32_t gpr = blocks_per_row >> 2;
+  const uint64_t row_code_bytes = (uint64_t)blocks_per_row * 8u;
 
-  for (uint32_t g0 = warp * (4u * kQuantUnroll); g0 < total_groups;
-       g0 += nwarps * (4u * kQuantUnroll)) {
-    uint4 v[kQuantUnroll];
-    uint32_t row[kQuantUnroll], gir[kQuantUnroll];
-    bool valid[kQuantUnroll], real[kQuantUnroll];
+  for (uint32_t base = warp; base < total_items; base += nwarps * kQuantUnroll) {
+    uint4 lo[kQuantUnroll], hi[kQuantUnroll];
+    uint32_t row[kQuantUnroll], blk[kQuantUnroll];
+    bool live[kQuantUnroll], real[kQuantUnroll];
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t g = g0 + u * 4u + (lane >> 3);
-      valid[u] = g < total_groups;
-      row[u] = valid[u] ? g / gpr : 0u;
-      gir[u] = valid[u] ? g - row[u] * gpr : 0u;
-      real[u] = valid[u] && row[u] < M;
-      v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (real[u]) v[u] = ld_nc_v4(x + row[u] * ldx + gir[u] * 64u + sub * 8u);
+      const uint32_t i = base + u * nwarps;                  // walk order
+      const bool in = i < total_items;
+      const uint32_t item = in ? total_items - 1u - i : 0u;  // reversed
+      row[u] = item / chunks_per_row;
+      blk[u] = (item - row[u] * chunks_per_row) * 32u + lane;
+      live[u] = in && blk[u] < blocks_per_row;
+      real[u] = live[u] && row[u] < M;
+      lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (real[u]) {
+        const __nv_bfloat16* src = x + row[u] * ldx + blk[u] * 16u;
+        lo[u] = ld_nc_v4(src);
+        hi[u] = ld_nc_v4(src + 8);
+      }
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const float own = absmax8(v[u]);
-      const float bamax = fmaxf(own, __shfl_xor_sync(0xFFFFFFFFu, own, 1));
-      const BlockScale bs = block_scale(bamax, ts, six_ts);
+      if (!live[u]) continue;
+      uint32_t scale = 0u;
       if (real[u]) {
-        const uint32_t word = bs.live ? encode8(v[u], bs.inv) : 0u;
-        *reinterpret_cast<uint32_t*>(codes + row[u] * row_code_bytes + gir[u] * 32u + sub * 4u) =
-            word;
+        const BlockScale bs = block_scale(fmaxf(absmax8(lo[u]), absmax8(hi[u])), ts, six_ts);
+        uint2 q = make_uint2(0u, 0u);
+        if (bs.live) q = make_uint2(encode8(lo[u], bs.inv), encode8(hi[u], bs.inv));
+        *reinterpret_cast<uint2*>(codes + row[u] * row_code_bytes + blk[u] * 8u) = q;
+        scale = bs.code;
       }
-      const uint32_t code = real[u] ? bs.code : 0u;
-      const uint32_t s0 = __shfl_sync(0xFFFFFFFFu, code, grp_lane0 + 0);
-      const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, code, grp_lane0 + 2);
-      const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, code, grp_lane0 + 4);
-      const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, code, grp_lane0 + 6);
-      if (sub == 0 && valid[u])
-        *reinterpret_cast<uint32_t*>(scales + scale_word_offset(row[u], gir[u], gpr)) =
-            s0 | (s1 << 8) | (s2 << 16) | (s3 << 24);
+      const uint32_t r = row[u], b = blk[u];
+      scales[((r >> 7) * gpr + (b >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (b & 3u)] =
+          static_cast<uint8_t>(scale);
     }
   }
 }
@@ -267,8 +263,7 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
   const uint32_t vpr = static_cast<uint32_t>(cols / 8);
   const uint32_t total = static_cast<uint32_t>(rows * (cols / 8));
   if (total == 0) return cudaSuccess;
-  const void* k = (ld == cols) ? (const void*)amax_kernel<true> : (const void*)amax_kernel<false>;
-  const int per_sm = resident_blocks(k, kAmaxThreads, 0);
+  static const int per_sm = resident_blocks((const void*)amax_kernel<true>, kAmaxThreads, 0);
   const uint32_t want = (total + kAmaxThreads * kAmaxUnroll - 1) / (kAmaxThreads * kAmaxUnroll);
   const uint32_t grid = std::min<uint32_t>(want, (uint32_t)(sm_count() * per_sm));
   if (ld == cols)
@@ -283,16 +278,17 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                             uint8_t* scales, const unsigned* amax_bits, const float* ts_in,
                             float* ts_out, cudaStream_t s) {
-  const uint32_t gpr = static_cast<uint32_t>(K / 64);
+  const uint32_t bpr = static_cast<uint32_t>(K / 16);
+  const uint32_t cpr = (bpr + 31u) / 32u;
   const int64_t mpad = (M + 127) / 128 * 128;
-  const uint32_t total = static_cast<uint32_t>(mpad * gpr);
-  const int per_sm = resident_blocks((const void*)quantize_kernel, kQuantThreads, 0);
-  const uint32_t groups_per_block = (kQuantThreads / 32) * 4u * kQuantUnroll;
-  const uint32_t want = (total + groups_per_block - 1) / groups_per_block;
+  const uint32_t total = static_cast<uint32_t>(mpad * cpr);
+  static const int per_sm = resident_blocks((const void*)quantize_kernel, kQuantThreads, 0);
+  const uint32_t items_per_block = (kQuantThreads / 32) * kQuantUnroll;
+  const uint32_t want = (total + items_per_block - 1) / items_per_block;
   const uint32_t grid = std::max<uint32_t>(1u, std::min<uint32_t>(want, (uint32_t)(sm_count() * per_sm)));
   quantize_kernel<<<grid, kQuantThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
                                                  static_cast<uint64_t>(ldx),
-                                                 static_cast<uint32_t>(M), gpr, total, codes,
+                                                 static_cast<uint32_t>(M), bpr, cpr, total, codes,
                                                  scales, amax_bits, ts_in, ts_out);
   return cudaGetLastError();
 }
