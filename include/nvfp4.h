@@ -184,6 +184,31 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status status);
 NVFP4_API nvfp4_status nvfp4_debug_wait_timeout(int *device_error, int64_t timeout_ns,
                                       nvfp4_stream_t stream);
 
+/*
+ * nvfp4_quantize_noalloc -- nvfp4_quantize (dynamic tensor scale) without a workspace
+ * argument, for callers that cannot allocate device memory. The pages have no counterpart:
+ * this is a packaging of the quantizer, not part of the method.
+ *
+ * Who needs it: a host framework's plugin interface that hands a kernel its inputs and
+ * outputs but no scratch buffer; a serving process that reserves all device memory in its
+ * own pool at start-up and forbids allocations afterwards; a latency-critical loop that
+ * must not call cudaMalloc/cudaFree, because those can synchronize the device or fail for
+ * lack of memory in the middle of a request.
+ *
+ * Arguments and results are those of nvfp4_quantize with tensor_scale_in = NULL. The
+ * scratch (the amax word) is a fixed 256-byte array inside the library, resident on every
+ * GPU that loads it until the process exits; the quantizer needs 16 bytes of it, and a
+ * need above 256 bytes would be refused with NVFP4_ERR_SHAPE. Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called. The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with that device
+ * current) and caches it; make that first call before any stream capture. Every call
+ * shares the array and clears the word it needs on `stream` before use, so calls that
+ * overlap on the GPU (different streams, or different host threads) race: serialize them.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_noalloc(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                              uint8_t *codes, uint8_t *scales,
+                                              float *tensor_scale, nvfp4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,7 @@ _SIGS = {
     "nvfp4_get_device_error": (ctypes.c_int, [_P, _P, _P]),
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
+    "nvfp4_quantize_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
 }
 
 
@@ -169,3 +170,17 @@ def nvfp4_get_device_error(device_error: torch.Tensor, stream=None) -> int:
 def nvfp4_debug_wait_timeout(device_error: torch.Tensor, timeout_ns: int, stream=None) -> None:
     _check("nvfp4_debug_wait_timeout", lib().nvfp4_debug_wait_timeout(
         _ptr(device_error), timeout_ns, _stream(stream)))
+
+
+def nvfp4_quantize_noalloc(x: torch.Tensor, out: Optional[Nvfp4Tensor] = None,
+                           stream=None) -> Nvfp4Tensor:
+    """nvfp4_quantize with a dynamic tensor scale, using the library's fixed scratch instead
+    of a workspace (for callers that cannot allocate; calls that overlap on the GPU race)."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        out = _alloc_nvfp4(M, K, x.device)
+    _check("nvfp4_quantize_noalloc", lib().nvfp4_quantize_noalloc(
+        _ptr(x), M, K, x.stride(0), _ptr(out.codes), _ptr(out.scales), _ptr(out.ts),
+        _stream(stream)))
+    return out
