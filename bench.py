@@ -93,25 +93,57 @@ def barrier(dist):
 # Clock sampling during the timed region (NVML, 10 ms period).
 # ---------------------------------------------------------------------------------------
 
+class _Nvml:
+    """Minimal ctypes binding of the NVML calls the sampler needs (libnvidia-ml.so.1)."""
+    CLOCK_SM = 1
+
+    def __init__(self, index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._ok(self.lib.nvmlInit_v2())
+        self.h = ctypes.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)))
+
+    def _ok(self, rc):
+        if rc != 0:
+            raise RuntimeError(f"NVML error {rc}")
+
+    def clock(self, max_clock=False) -> int:
+        v = self.c.c_uint()
+        f = self.lib.nvmlDeviceGetMaxClockInfo if max_clock else self.lib.nvmlDeviceGetClockInfo
+        self._ok(f(self.h, self.c.c_int(self.CLOCK_SM), self.c.byref(v)))
+        return int(v.value)
+
+    def reasons(self) -> int:
+        v = self.c.c_ulonglong()
+        f = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._ok(f(self.h, self.c.byref(v)))
+        return int(v.value)
+
+
 class ClockSampler:
+    """Samples the SM clock and the clock-event (throttle) reasons every `period_s` during the
+    timed region, through NVML (ctypes); falls back to nvidia-smi if NVML cannot be loaded."""
     REASONS = {
         "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
         "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
     }
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int, period_s: float = 0.01):
+    def __init__(self, index: int, period_s: float = 0.002):
         self.samples, self.reasons, self.max_mhz = [], set(), None
         self.period = period_s
         self.error = None
         self.index = index
         self._stop = threading.Event()
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # no NVML: fall back to one nvidia-smi query per sample
+            self.nv = _Nvml(index)
+            self.max_mhz = self.nv.clock(max_clock=True)
+        except Exception as e:
             self.nv = None
             self.error = f"nvml: {type(e).__name__}: {e}"
 
@@ -120,15 +152,11 @@ class ClockSampler:
             self._sample()
             time.sleep(self.period)
 
-    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-                  "clocks_event_reasons.sw_power_cap")
-
     def _sample(self):
         try:
             if self.nv is not None:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                self.samples.append(self.nv.clock())
+                r = self.nv.reasons()
                 for name, bit in self.REASONS.items():
                     if r & bit:
                         self.reasons.add(name)
@@ -159,6 +187,7 @@ class ClockSampler:
 
     def summary(self):
         s = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+             "sm_min_mhz": min(self.samples) if self.samples else None,
              "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
              "samples": len(self.samples), "source": "nvml" if self.nv is not None else "nvidia-smi"}
         if self.error:
@@ -329,6 +358,7 @@ def run_ours(args, world, rank, local):
                      "frac_of_15pf": round(achieved / (NOMINAL_FP4_PF * 1e3), 4),
                      "traffic": traffic, "algorithmic_bytes": dom_bytes},
         "gemm_only_tflops": round(flops_step / (gemm_ms / 1e3) / 1e12, 1),
+        "step_ms_min_median": [round(float(step_ms.min()), 5), round(float(np.median(step_ms)), 5)],
         "breakdown": breakdown,
         "gpu_launches": kernels_per_step * K,
         "clocks": clocks.summary(),

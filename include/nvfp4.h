@@ -86,7 +86,11 @@ NVFP4_API size_t nvfp4_scales_bytes(int64_t rows, int64_t K);
  * 512-byte tile). Returns -1 for out-of-range arguments. */
 NVFP4_API int64_t nvfp4_scale_offset(int64_t row, int64_t kblock, int64_t K);
 
-/* Bytes of scratch `workspace` that nvfp4_quantize / nvfp4_pack_weights need (16). */
+/* Bytes of scratch `workspace` that nvfp4_quantize / nvfp4_pack_weights need (16).
+ * nvfp4_quantize expects the workspace zero-filled before its first use and leaves it
+ * zero-filled again (its amax word and a finished-CTA count), so allocate and zero it once
+ * and reuse it; nvfp4_pack_weights also leaves it zero-filled. Calls that use the same
+ * workspace must not overlap on the GPU. */
 NVFP4_API size_t nvfp4_workspace_bytes(void);
 
 /*
@@ -100,8 +104,11 @@ NVFP4_API size_t nvfp4_workspace_bytes(void);
  *   tensor_scale_in  optional fp32 [1] device pointer. NULL: ts = amax(|x|) / 2688 of this
  *            x (dynamic per call; costs one extra read of x). Non-NULL: that static ts is
  *            used and x is read once.
- *   workspace  >= nvfp4_workspace_bytes() device bytes, 16-byte aligned (amax scratch);
- *            may be NULL when tensor_scale_in is given.
+ *   workspace  >= nvfp4_workspace_bytes() device bytes, 16-byte aligned, zero-filled
+ *            before its first use and then reused (see nvfp4_workspace_bytes); may be NULL
+ *            when tensor_scale_in is given.
+ * Two launches: an amax pass over x (skipped for a static scale), then the quantize pass,
+ * which walks x backwards so that what the amax pass read last is still in L2.
  * Per block of 16: s = E4M3(bamax / fp32(6 ts)) (nearest even, saturating at 448);
  * d = fp32(dec(s) ts); if d < 2^-126 the block stores scale 0 and codes +0; otherwise each
  * element is coded E2M1(fp32(x * fp32(1/d))) (nearest even, saturating at 6; a negative
@@ -196,14 +203,15 @@ NVFP4_API nvfp4_status nvfp4_debug_wait_timeout(int *device_error, int64_t timeo
  * lack of memory in the middle of a request.
  *
  * Arguments and results are those of nvfp4_quantize with tensor_scale_in = NULL. The
- * scratch (the amax word) is a fixed 256-byte array inside the library, resident on every
- * GPU that loads it until the process exits; the quantizer needs 16 bytes of it, and a
- * need above 256 bytes would be refused with NVFP4_ERR_SHAPE. Nothing is allocated: no
- * cudaMalloc, cudaFree or allocating library routine is called. The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress, with that device
- * current) and caches it; make that first call before any stream capture. Every call
- * shares the array and clears the word it needs on `stream` before use, so calls that
- * overlap on the GPU (different streams, or different host threads) race: serialize them.
+ * scratch (the amax word and a finished-CTA count) is a fixed 256-byte array inside the
+ * library, resident on every GPU that loads it until the process exits; the quantizer
+ * needs 16 bytes of it, and a need above 256 bytes would be refused with NVFP4_ERR_SHAPE.
+ * Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine is called.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current) and caches it; make that first call before any stream
+ * capture. Every call shares the array and zeroes the 16 bytes it uses on `stream` before
+ * the quantizer runs, so calls that overlap on the GPU (different streams, or different
+ * host threads) race: serialize them.
  */
 NVFP4_API nvfp4_status nvfp4_quantize_noalloc(const void *x, int64_t M, int64_t K, int64_t ldx,
                                               uint8_t *codes, uint8_t *scales,

@@ -117,7 +117,7 @@ def nvfp4_quantize(x: torch.Tensor, tensor_scale_in: Optional[torch.Tensor] = No
     if out is None:
         out = _alloc_nvfp4(M, K, x.device)
     if workspace is None and tensor_scale_in is None:
-        workspace = torch.empty(nvfp4_workspace_bytes(), dtype=torch.uint8, device=x.device)
+        workspace = torch.zeros(nvfp4_workspace_bytes(), dtype=torch.uint8, device=x.device)
     _check("nvfp4_quantize", lib().nvfp4_quantize(
         _ptr(x), M, K, x.stride(0), _ptr(out.codes), _ptr(out.scales), _ptr(out.ts),
         _ptr(tensor_scale_in), _ptr(workspace), _stream(stream)))
@@ -133,7 +133,7 @@ def nvfp4_pack_weights(w: torch.Tensor, gated_interleave: bool = False,
     if out is None:
         out = _alloc_nvfp4(N, K, w.device)
     if workspace is None:
-        workspace = torch.empty(nvfp4_workspace_bytes(), dtype=torch.uint8, device=w.device)
+        workspace = torch.zeros(nvfp4_workspace_bytes(), dtype=torch.uint8, device=w.device)
     _check("nvfp4_pack_weights", lib().nvfp4_pack_weights(
         _ptr(w), K, N, int(bool(gated_interleave)), _ptr(out.codes), _ptr(out.scales),
         _ptr(out.ts), _ptr(workspace), _stream(stream)))

@@ -119,12 +119,8 @@ nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
     return NVFP4_ERR_ALIGN;
   if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  unsigned* amax = static_cast<unsigned*>(workspace);
-  if (tensor_scale_in == nullptr) {
-    if (cudaMemsetAsync(amax, 0, sizeof(unsigned), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
-    if (nvfp4_status st = from_cuda(nvfp4::launch_amax(x, M, K, ldx, amax, s)); st != NVFP4_OK) return st;
-  }
-  return from_cuda(nvfp4::launch_quantize(x, M, K, ldx, codes, scales, amax, tensor_scale_in, tensor_scale, s));
+  return from_cuda(nvfp4::launch_quantize(x, M, K, ldx, codes, scales, static_cast<unsigned*>(workspace),
+                                          tensor_scale_in, tensor_scale, s));
 }
 
 nvfp4_status nvfp4_pack_weights(const void* w, int64_t K, int64_t N, int gated_interleave, uint8_t* codes,
@@ -140,10 +136,15 @@ nvfp4_status nvfp4_pack_weights(const void* w, int64_t K, int64_t N, int gated_i
   if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   unsigned* amax = static_cast<unsigned*>(workspace);
-  if (cudaMemsetAsync(amax, 0, sizeof(unsigned), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  if (cudaMemsetAsync(amax, 0, nvfp4_workspace_bytes(), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
   if (cudaMemsetAsync(scales, 0, nvfp4_scales_bytes(N, K), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
   if (nvfp4_status st = from_cuda(nvfp4::launch_amax(w, K, N, N, amax, s)); st != NVFP4_OK) return st;
-  return from_cuda(nvfp4::launch_pack_weights(w, K, N, gated_interleave == 1, codes, scales, amax, tensor_scale, s));
+  if (nvfp4_status st = from_cuda(nvfp4::launch_pack_weights(w, K, N, gated_interleave == 1, codes, scales,
+                                                               amax, tensor_scale, s));
+      st != NVFP4_OK)
+    return st;
+  // leave the workspace zeroed, the state nvfp4_quantize expects of a fresh workspace
+  return from_cuda(cudaMemsetAsync(amax, 0, nvfp4_workspace_bytes(), s));
 }
 
 nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_ts,

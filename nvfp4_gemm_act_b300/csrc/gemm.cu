@@ -7,19 +7,29 @@
 // trailing small op fused into the epilogue (bias; per-head RMSNorm with head_dim 256;
 // gated-SiLU "SiLU(C[:, :N//2]) * C[:, N//2:]" over weight columns paired at packing time).
 //
-// Design: a persistent kernel, one CTA per SM, each CTA walking 128 x 256 output tiles
-// (static round-robin over tiles, row tiles fastest so concurrent CTAs share weight tiles).
-//   warp 0     TMA producer: A/B code tiles (128-byte swizzle) and the scale tiles (1-D bulk
-//              copies) into a 4-stage shared-memory ring; it also prefetches the k-blocks
-//              8 ahead into L2, so the ring is fed from L2 rather than DRAM latency;
-//   warp 1     allocates TMEM; one thread copies each stage's scales shared -> TMEM
-//              (tcgen05.cp) and issues tcgen05.mma kind::mxf4nvf4 (M128 N256 K64, UE4M3
-//              scale per 16) into the fp32 accumulator, then frees the stage (tcgen05.commit);
-//   warps 2-9  epilogue: TMEM lane = output row; two warps per 32-lane quarter, one per
-//              128-column half. Each thread pulls its 128 accumulator columns into registers
-//              and releases TMEM at once, so the next tile's MMAs run while it applies the
-//              epilogue and stores. Per-head RMSNorm sums are thread-local, combined across
-//              the two halves through shared memory when a head spans the whole tile.
+// Design: a persistent kernel launched as CTA pairs (clusters of 2, one CTA per SM). A pair
+// computes 256 x 256 output tiles with the 2-SM MMA (tcgen05.mma.cta_group::2, M256 N256
+// K64): CTA r owns rows [128 r, 128 r + 128) of the tile and holds only half of the weight
+// tile, so a 256-deep pipeline stage is 38 KB per SM (5 stages in flight). Pairs walk
+// (row-tile pair, weight tile) tiles round-robin, row pairs fastest, so concurrent pairs
+// share weight tiles in L2.
+//   warp 0     (both CTAs) TMA producer: this CTA's A tile, its half of the B tile, its A
+//              scale tile and both B scale bands (every CTA needs the scales of all 256
+//              columns in its TMEM); all of them complete on the leader CTA's full barrier;
+//              L2 prefetch 8 k-blocks ahead;
+//   warp 1     (both CTAs) TMEM allocation (pair-collective); in the leader, the single
+//              MMA-issuing thread, whose commits release the stage and publish the
+//              accumulator in both CTAs;
+//   warps 2-3  (leader) block-scale copies shared -> TMEM (tcgen05.cp.cta_group::2 copies
+//              each CTA's own shared block into its own TMEM), split between two warps and
+//              running a stage ahead of the MMA warp: a copy costs its issuing thread about
+//              as long as an MMA, so the MMA thread must not issue them;
+//   warps 4-11 (both CTAs) epilogue: TMEM lane = output row; two warps per 32-lane quarter,
+//              one per 128-column half. Each thread pulls its 128 accumulator columns into
+//              registers, then reports TMEM free to the leader, so the next tile's MMAs run
+//              while it applies the epilogue and stores. Per-head RMSNorm sums are
+//              thread-local, combined across the two halves through shared memory when a
+//              head spans the whole tile.
 // Every wait is bounded (NVFP4_ERR_TIMEOUT in *err on expiry; the CTA then drains what it
 // issued, frees TMEM and exits).
 
@@ -36,25 +46,31 @@
 namespace nvfp4 {
 namespace {
 
-constexpr int kBM = 128;                 // rows of A per tile (TMEM lanes)
+constexpr int kBM = 128;                 // rows of A per CTA (TMEM lanes)
 constexpr int kBN = 256;                 // columns of the tile (TMEM accumulator columns)
 constexpr int kBK = 256;                 // K elements per pipeline stage
 constexpr int kBKBytes = kBK / 2;        // 128: one 128-byte swizzle row of packed E2M1
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kMmaK = 64;                // K per tcgen05.mma (kind::mxf4nvf4)
 constexpr int kKStepsPerStage = kBK / kMmaK;
 constexpr int kPrefetchDist = 8;         // k-blocks prefetched into L2 ahead of the ring
+constexpr int kCluster = 2;              // the CTA pair of the 2-SM MMA
+constexpr int kBRowsPerCta = kBN / kCluster;
 
 constexpr int kABytes = kBM * kBKBytes;                       // 16 KB
-constexpr int kBBytes = kBN * kBKBytes;                       // 32 KB
+constexpr int kBBytes = kBRowsPerCta * kBKBytes;              // 16 KB (this CTA's half)
 constexpr int kSfAtom = 512;                                  // 128 rows x 4 scales
-constexpr int kSfaBytes = (kBM / 128) * kKStepsPerStage * kSfAtom;  // 2 KB
-constexpr int kSfbBytes = (kBN / 128) * kKStepsPerStage * kSfAtom;  // 4 KB
+constexpr int kSfaBytes = kKStepsPerStage * kSfAtom;          // 2 KB
+constexpr int kSfbBytes = (kBN / 128) * kKStepsPerStage * kSfAtom;  // 4 KB: both bands
+constexpr int kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // bytes per CTA per stage
 
+constexpr int kSfWarps = 2;              // warps issuing the scale copies (shared -> TMEM)
+constexpr int kEpiWarp0 = 2 + kSfWarps;  // first epilogue warp
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kThreads = kEpiWarp0 * 32 + kEpiThreads;
 constexpr int kHalf = kBN / 2;           // columns per epilogue warp
+static_assert(kEpiWarp0 % 4 == 0, "epilogue warps must start on a warpgroup (TMEM lane quarters)");
 
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
@@ -64,7 +80,9 @@ constexpr int kOffParam = kOffSfb + kStages * kSfbBytes;      // bias / gamma, d
 constexpr int kParamBytes = 2 * 2 * kBN * 4;
 constexpr int kOffXch = kOffParam + kParamBytes;              // RMSNorm half-row sums
 constexpr int kXchBytes = 2 * kBM * 4;
-constexpr int kOffFlags = kOffXch + kXchBytes;                // epilogue wait results
+constexpr int kOffEpiBuf = kOffXch + kXchBytes;               // per-warp store staging
+constexpr int kEpiBufBytes = 32 * 64;                         // 32 rows x 64 bytes per warp
+constexpr int kOffFlags = kOffEpiBuf + kEpiWarps * kEpiBufBytes;  // epilogue wait results
 constexpr int kOffBar = kOffFlags + 64;
 constexpr int kBarBytes = 256;
 constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;        // + slack to align to 1 KB
@@ -86,7 +104,7 @@ constexpr uint32_t make_idesc(int m, int n) {
   return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
-constexpr uint32_t kIdesc = make_idesc(kBM, kBN);
+constexpr uint32_t kIdesc = make_idesc(kCluster * kBM, kBN);
 
 struct EpiParams {
   const float* a_ts;
@@ -104,41 +122,81 @@ struct EpiParams {
   int out_fp32;
 };
 
-// Stores NV consecutive values of one output row (col multiple of 8, 16-byte aligned rows).
+// Stores this warp's 32 rows x NV values (thread = row, y[] = its values, columns
+// [col0, col0 + NV) of the output) through the warp's 2 KB shared buffer: each lane writes
+// its row's next 64 bytes (16-byte pieces XOR-swizzled by row pair, so the row-per-lane
+// writes hit distinct banks), then each global store instruction writes 8 rows x 64
+// contiguous bytes instead of 32 scattered 16-byte pieces.
 template <int NV>
-__device__ __forceinline__ void store_row(const EpiParams& p, int row, int col, const float* y) {
-  if (p.out_fp32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col);
+__device__ __forceinline__ void store_rows(const EpiParams& p, const float* y, int row0, int col0,
+                                           int width, uint32_t buf, int lane) {
+  const bool bf16 = !p.out_fp32;
+  const int per_chunk = bf16 ? 32 : 16;  // values per 64-byte row segment
+  const int swz_w = (lane >> 1) & 3;
 #pragma unroll
-    for (int i = 0; i < NV / 4; ++i) dst[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
-  } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col);
+  for (int c = 0; c < NV; c += 16) {
+    // write: 64 bytes of this lane's row (bf16: 32 values; fp32: 16 values)
+    if (bf16) {
+      if ((c & 31) != 0) continue;  // bf16 chunks are 32 values; handled at c % 32 == 0
 #pragma unroll
-    for (int i = 0; i < NV / 8; ++i)
-      dst[i] = make_uint4(pack_bf16x2(y[8 * i], y[8 * i + 1]), pack_bf16x2(y[8 * i + 2], y[8 * i + 3]),
-                          pack_bf16x2(y[8 * i + 4], y[8 * i + 5]), pack_bf16x2(y[8 * i + 6], y[8 * i + 7]));
+      for (int piece = 0; piece < 4; ++piece) {
+        const float* v = y + c + piece * 8;
+        const uint4 w = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                   pack_bf16x2(v[6], v[7]));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 64 + ((piece ^ swz_w) * 16)),
+                     "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
+                     : "memory");
+      }
+    } else {
+#pragma unroll
+      for (int piece = 0; piece < 4; ++piece) {
+        const float* v = y + c + piece * 4;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 64 + ((piece ^ swz_w) * 16)),
+                     "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                     "r"(__float_as_uint(v[3]))
+                     : "memory");
+      }
+    }
+    __syncwarp();
+    // read back row-contiguous and store: lane -> (row r = i * 8 + lane / 4, piece lane % 4)
+    const int piece = lane & 3;
+    const int col = col0 + c + piece * (bf16 ? 8 : 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 8 + (lane >> 2);
+      uint4 w;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                   : "r"(buf + r * 64 + ((piece ^ ((r >> 1) & 3)) * 16))
+                   : "memory");
+      const int row = row0 + r;
+      if (row < p.M && col < width) {
+        if (bf16)
+          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col) = w;
+        else
+          *reinterpret_cast<uint4*>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col) = w;
+      }
+    }
+    __syncwarp();
+    (void)per_chunk;
   }
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
-  return g * __frcp_rn(1.0f + __expf(-g)) * u;
+  // sigma(g) = 1 / (1 + e^-g); __fdividef returns 0 once the denominator exceeds 2^126
+  return g * __fdividef(1.0f, 1.0f + __expf(-g)) * u;
 }
 
 // Epilogue of one thread: its row's 128 columns [c0, c0 + 128) of the tile, already in z
 // (z = alpha * acc + bias). `xch` is the shared half-row exchange (RMSNorm, head 256).
-__device__ __forceinline__ void epilogue_row(const EpiParams& p, float (&z)[kHalf], int row, int c0,
-                                             int half, int row_local, const float* gamma_s,
-                                             float* xch) {
-  const bool live = row < p.M;
+__device__ __forceinline__ void epilogue_row(const EpiParams& p, float (&z)[kHalf], int row0, int c0,
+                                             int half, int row_local, const float* gamma_s, float* xch,
+                                             uint32_t buf, int lane) {
   if (p.epi == NVFP4_EPI_GATED_SILU) {
     float y[kHalf / 2];
 #pragma unroll
     for (int j = 0; j < kHalf / 2; ++j) y[j] = silu_mul(z[2 * j], z[2 * j + 1]);
-    if (live) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (c0 + c * 32 < p.N) store_row<16>(p, row, (c0 + c * 32) >> 1, y + c * 16);
-    }
+    store_rows<kHalf / 2>(p, y, row0, c0 >> 1, p.N >> 1, buf, lane);
     return;
   }
   if (p.epi == NVFP4_EPI_HEAD_RMSNORM) {
@@ -178,112 +236,156 @@ __device__ __forceinline__ void epilogue_row(const EpiParams& p, float (&z)[kHal
       }
     }
   }
-  if (live) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      if (c0 + c * 32 < p.N) store_row<32>(p, row, c0 + c * 32, z + c * 32);
-  }
+  store_rows<kHalf>(p, z, row0, c0, p.N, buf, lane);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                      const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb, int K,
-                      int num_m_blocks, int num_tiles, EpiParams ep, int* err, uint64_t timeout_ns) {
+                      const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
+                      int K, int num_m_blocks, int num_tiles, EpiParams ep, int* err, uint64_t timeout_ns) {
+  // num_tiles counts pair tiles: (row-tile pair, weight tile); row pairs fastest.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  // bars[0..S): full, [S..2S): empty, [2S]: accumulator full, [2S+1]: accumulator empty,
-  // [2S+2]: MMA drain
+  // bars[0..S): full (used in the leader), [S..2S): empty, [2S..3S): scales in TMEM (leader),
+  // [3S]: accumulator full, [3S+1]: accumulator empty (leader), [3S+2]: MMA drain,
+  // [3S+3]: scale-copy drain
   auto full_bar = [&](int s) { return smem_u32(bars + s); };
   auto empty_bar = [&](int s) { return smem_u32(bars + kStages + s); };
-  const uint32_t acc_full_bar = smem_u32(bars + 2 * kStages);
-  const uint32_t acc_empty_bar = smem_u32(bars + 2 * kStages + 1);
-  const uint32_t drain_bar = smem_u32(bars + 2 * kStages + 2);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 3);
+  auto sf_bar = [&](int s) { return smem_u32(bars + 2 * kStages + s); };
+  const uint32_t acc_full_bar = smem_u32(bars + 3 * kStages);
+  const uint32_t acc_empty_bar = smem_u32(bars + 3 * kStages + 1);
+  const uint32_t drain_bar = smem_u32(bars + 3 * kStages + 2);
+  const uint32_t sf_drain_bar = smem_u32(bars + 3 * kStages + 3);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_k_blocks = (K + kBK - 1) / kBK;
   const int k_atoms = K / 64;                       // scale tiles per 128-row band
-  const int sfb_bands = (ep.N + 127) / 128;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
+  const int cluster_id = blockIdx.x / kCluster;
+  const int num_clusters = gridDim.x / kCluster;
+  const int num_pairs_m = (num_m_blocks + kCluster - 1) / kCluster;
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
+    prefetch_tmap(&tm_sfa);
+    prefetch_tmap(&tm_sfb);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(full_bar(s), 1);            // the leader's producer arrival (+ both CTAs' bytes)
+      mbar_init(empty_bar(s), 1);           // the leader's MMA commit
+      mbar_init(sf_bar(s), kSfWarps);       // one commit from each scale-copy warp
     }
     mbar_init(acc_full_bar, 1);
-    mbar_init(acc_empty_bar, kEpiWarps);
+    mbar_init(acc_empty_bar, kCluster * kEpiWarps);  // every epilogue warp of both CTAs
     mbar_init(drain_bar, 1);
+    mbar_init(sf_drain_bar, kSfWarps);
     fence_mbarrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated, before any signal
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (both CTAs) ----------------
       const uint64_t pol = policy_evict_normal();
       uint32_t kc = 0;  // k-blocks issued so far (ring position)
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m_blk = tile % num_m_blocks;
-        const int n_blk = tile / num_m_blocks;
-        const int halves = (n_blk * 2 + 1 < sfb_bands) ? 2 : 1;
+      for (int pt = cluster_id; pt < num_tiles && ok; pt += num_clusters) {
+        const int m_blk = (pt % num_pairs_m) * kCluster + rank;  // rows past M load as zeros
+        const int n_blk = pt / num_pairs_m;
+        const int b_row = n_blk * kBN + rank * kBRowsPerCta;
         for (int kb = 0; kb < min(num_k_blocks, kPrefetchDist); ++kb) {
           tma_prefetch_2d(&tm_a, kb * kBKBytes, m_blk * kBM);
-          tma_prefetch_2d(&tm_b, kb * kBKBytes, n_blk * kBN);
+          tma_prefetch_2d(&tm_b, kb * kBKBytes, b_row);
         }
         for (int kb = 0; kb < num_k_blocks; ++kb) {
           if (kb + kPrefetchDist < num_k_blocks) {
             tma_prefetch_2d(&tm_a, (kb + kPrefetchDist) * kBKBytes, m_blk * kBM);
-            tma_prefetch_2d(&tm_b, (kb + kPrefetchDist) * kBKBytes, n_blk * kBN);
+            tma_prefetch_2d(&tm_b, (kb + kPrefetchDist) * kBKBytes, b_row);
           }
           const int s = kc % kStages;
           if (!mbar_wait(empty_bar(s), ((kc / kStages) & 1u) ^ 1u, timeout_ns, err)) {
             ok = false;
             break;
           }
-          const int nk = min(kKStepsPerStage, k_atoms - kb * kKStepsPerStage);
-          const uint32_t sf_bytes = static_cast<uint32_t>(nk * kSfAtom);
-          mbar_arrive_expect_tx(full_bar(s), kABytes + kBBytes + sf_bytes * (1 + halves));
-          tma_load_2d(sbase + kOffA + s * kABytes, &tm_a, kb * kBKBytes, m_blk * kBM, full_bar(s), pol);
-          tma_load_2d(sbase + kOffB + s * kBBytes, &tm_b, kb * kBKBytes, n_blk * kBN, full_bar(s), pol);
-          bulk_load(sbase + kOffSfa + s * kSfaBytes,
-                    sfa + ((size_t)m_blk * k_atoms + (size_t)kb * kKStepsPerStage) * kSfAtom, sf_bytes,
-                    full_bar(s));
-          for (int h = 0; h < halves; ++h)
-            bulk_load(sbase + kOffSfb + s * kSfbBytes + h * (kSfbBytes / 2),
-                      sfb + ((size_t)(n_blk * 2 + h) * k_atoms + (size_t)kb * kKStepsPerStage) * kSfAtom,
-                      sf_bytes, full_bar(s));
+          const uint32_t bar = mapa_shared(full_bar(s), 0);  // the leader's full barrier
+          if (leader) mbar_arrive_expect_tx(full_bar(s), kCluster * kStageTx);
+          tma_load_2d_pair(sbase + kOffA + s * kABytes, &tm_a, kb * kBKBytes, m_blk * kBM, bar, pol);
+          tma_load_2d_pair(sbase + kOffB + s * kBBytes, &tm_b, kb * kBKBytes, b_row, bar, pol);
+          // scale tiles: row = band * k_atoms + first k-atom of the stage (4 atoms of 512 B)
+          tma_load_2d_pair(sbase + kOffSfa + s * kSfaBytes, &tm_sfa, 0,
+                           m_blk * k_atoms + kb * kKStepsPerStage, bar, pol);
+          for (int h = 0; h < kBN / 128; ++h)
+            tma_load_2d_pair(sbase + kOffSfb + s * kSfbBytes + h * (kSfbBytes / 2), &tm_sfb, 0,
+                             (n_blk * 2 + h) * k_atoms + kb * kKStepsPerStage, bar, pol);
           ++kc;
         }
       }
-      // Make sure no copy into this CTA's shared memory is still in flight at exit.
+      // Before exit: the leader's MMA has released every stage this CTA filled, so all its
+      // copies have landed and all the leader's arrivals on this CTA's barriers are made.
       for (uint32_t i = kc > (uint32_t)kStages ? kc - kStages : 0u; i < kc; ++i)
-        (void)mbar_wait(full_bar(i % kStages), (i / kStages) & 1u, timeout_ns, err);
+        (void)mbar_wait(empty_bar(i % kStages), (i / kStages) & 1u, timeout_ns, err);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (leader) ----------------
       uint32_t kc = 0;
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
-        const int n_blk = tile / num_m_blocks;
-        const int halves = (n_blk * 2 + 1 < sfb_bands) ? 2 : 1;
-        // the epilogue has pulled the previous tile's accumulator out of TMEM
+      for (int pt = cluster_id; pt < num_tiles && ok; pt += num_clusters, ++it) {
+        // both CTAs' epilogues have pulled the previous accumulator out of TMEM
         if (!mbar_wait(acc_empty_bar, (it & 1u) ^ 1u, timeout_ns, err)) break;
         tc_fence_after();
+        for (int kb = 0; kb < num_k_blocks; ++kb) {
+          const int s = kc % kStages;
+          // operands of both CTAs landed, and their scales are in both TMEMs
+          if (!mbar_wait(full_bar(s), (kc / kStages) & 1u, timeout_ns, err) ||
+              !mbar_wait(sf_bar(s), (kc / kStages) & 1u, timeout_ns, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nk = min(kKStepsPerStage, k_atoms - kb * kKStepsPerStage);
+          const uint32_t sf_col = tmem_base + kSfCol0 + s * kSfColsPerStage;
+          const uint32_t a_s = sbase + kOffA + s * kABytes;
+          const uint32_t b_s = sbase + kOffB + s * kBBytes;
+          for (int j = 0; j < nk; ++j) {
+            const uint64_t adesc = smem_desc(a_s + j * (kMmaK / 2), 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = smem_desc(b_s + j * (kMmaK / 2), 16, 1024, kSwizzle128B);
+            mma_nvf4_pair(tmem_base + kAccCol, adesc, bdesc, kIdesc, sf_col + j * 4,
+                          sf_col + kSfaColsPerStage + j * 8, (kb | j) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(empty_bar(s), 0x3);  // release the stage in both CTAs
+          ++kc;
+        }
+        if (ok) tc_commit_pair_mc(acc_full_bar, 0x3);
+      }
+      // Drain: every MMA issued has finished before TMEM is released.
+      tc_commit_pair(drain_bar);
+      (void)mbar_wait(drain_bar, 0u, timeout_ns, err);
+    }
+  } else if (warp < kEpiWarp0) {
+    if (lane == 0 && leader) {
+      // ---------------- block-scale copies, shared -> TMEM (leader, for both CTAs) --------
+      // scale warp w copies, per 64-deep k-step, B scale band w and the A scales of
+      // k-steps {2w, 2w+1}; the TMEM slot of stage s is free again once stage s has been
+      // refilled (the refill waited for the MMAs that read the previous scales).
+      const int w = warp - 2;
+      uint32_t kc = 0;
+      bool ok = true;
+      for (int pt = cluster_id; pt < num_tiles && ok; pt += num_clusters) {
         for (int kb = 0; kb < num_k_blocks; ++kb) {
           const int s = kc % kStages;
           if (!mbar_wait(full_bar(s), (kc / kStages) & 1u, timeout_ns, err)) {
@@ -296,35 +398,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sfa_s = sbase + kOffSfa + s * kSfaBytes;
           const uint32_t sfb_s = sbase + kOffSfb + s * kSfbBytes;
           for (int j = 0; j < nk; ++j) {
-            tmem_cp_32x128b_x4(sf_col + j * 4, smem_desc(sfa_s + j * kSfAtom, 128, 128, kSwizzleNone));
-            for (int h = 0; h < halves; ++h)
-              tmem_cp_32x128b_x4(sf_col + kSfaColsPerStage + j * 8 + h * 4,
-                                 smem_desc(sfb_s + h * (kSfbBytes / 2) + j * kSfAtom, 128, 128, kSwizzleNone));
+            if ((j >> 1) == w)
+              tmem_cp_32x128b_x4_pair(sf_col + j * 4, smem_desc(sfa_s + j * kSfAtom, 128, 128, kSwizzleNone));
+            tmem_cp_32x128b_x4_pair(sf_col + kSfaColsPerStage + j * 8 + w * 4,
+                                    smem_desc(sfb_s + w * (kSfbBytes / 2) + j * kSfAtom, 128, 128, kSwizzleNone));
           }
-          const uint32_t a_s = sbase + kOffA + s * kABytes;
-          const uint32_t b_s = sbase + kOffB + s * kBBytes;
-          for (int j = 0; j < nk; ++j) {
-            const uint64_t adesc = smem_desc(a_s + j * (kMmaK / 2), 16, 1024, kSwizzle128B);
-            const uint64_t bdesc = smem_desc(b_s + j * (kMmaK / 2), 16, 1024, kSwizzle128B);
-            mma_nvf4(tmem_base + kAccCol, adesc, bdesc, kIdesc, sf_col + j * 4,
-                     sf_col + kSfaColsPerStage + j * 8, (kb | j) != 0 ? 1u : 0u);
-          }
-          tc_commit(empty_bar(s));
+          tc_commit_pair(sf_bar(s));
           ++kc;
         }
-        if (ok) tc_commit(acc_full_bar);
       }
-      // Drain: every MMA this thread issued has finished before TMEM is released.
-      tc_commit(drain_bar);
-      (void)mbar_wait(drain_bar, 0u, timeout_ns, err);
+      tc_commit_pair(sf_drain_bar);
+      (void)mbar_wait(sf_drain_bar, 0u, timeout_ns, err);
     }
   } else {
-    // ---------------- epilogue warps ----------------
-    const int ew = warp - 2;               // 0..7
+    // ---------------- epilogue warps (both CTAs) ----------------
+    const int ew = warp - kEpiWarp0;       // 0..7
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int half = ew >> 2;              // which 128-column half of the tile
     const int et = ew * 32 + lane;         // 0..255
     const int row_local = q * 32 + lane;
+    const uint32_t leader_acc_empty = mapa_shared(acc_empty_bar, 0);
     float* param = reinterpret_cast<float*>(smem + kOffParam);
     float* xch = reinterpret_cast<float*>(smem + kOffXch);
     volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
@@ -332,9 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool gated = ep.epi == NVFP4_EPI_GATED_SILU;
     const int nhalf = ep.N >> 1;
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-      const int m_blk = tile % num_m_blocks;
-      const int n_blk = tile / num_m_blocks;
+    for (int pt = cluster_id; pt < num_tiles; pt += num_clusters, ++it) {
+      const int m_blk = (pt % num_pairs_m) * kCluster + rank;  // rows past M are not stored
+      const int n_blk = pt / num_pairs_m;
       const int n_base = n_blk * kBN;
       // per-column parameters of this tile -> shared memory (buffer it & 1)
       float* bias_s = param + (it & 1u) * (2 * kBN);
@@ -369,24 +462,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32cols(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(r + 96));
         tmem_ld_wait();
       }
-      // accumulator is in registers: hand TMEM back to the MMA warp
+      // accumulator is in registers: tell the leader's MMA warp this TMEM is free
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty_bar);
+      if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
       const float* bh = bias_s + half * kHalf;
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) z[i] = fmaf(alpha, z[i], bh[i]);
-      const int row = m_blk * kBM + row_local;
-      epilogue_row(ep, z, row, n_base + half * kHalf, half, row_local, gamma_s + half * kHalf, xch);
+      epilogue_row(ep, z, m_blk * kBM + q * 32, n_base + half * kHalf, half, row_local, gamma_s + half * kHalf,
+                   xch, sbase + kOffEpiBuf + ew * kEpiBufBytes, lane);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // neither CTA of the pair leaves while the other may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -416,12 +510,29 @@ bool encode_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The tiled scale buffer seen as 32-bit words [atoms, 128]: one 512-byte atom per row,
+// atoms ordered (128-row band, k-atom) with k-atoms fastest. A stage loads 4 atoms.
+bool encode_scales_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
+  auto fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t atoms = static_cast<cuuint64_t>((rows + 127) / 128) * static_cast<cuuint64_t>(K / 64);
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kSfAtom / 4), atoms};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kSfAtom)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kSfAtom / 4), static_cast<cuuint32_t>(kKStepsPerStage)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  CUtensorMap tm_a, tm_b;
+  CUtensorMap tm_a, tm_b, tm_sfa, tm_sfb;
   if (!encode_codes_map(&tm_a, a.a_codes, a.M, a.K, kBM)) return NVFP4_ERR_LAUNCH;
-  if (!encode_codes_map(&tm_b, a.b_codes, a.N, a.K, kBN)) return NVFP4_ERR_LAUNCH;
+  if (!encode_codes_map(&tm_b, a.b_codes, a.N, a.K, kBRowsPerCta)) return NVFP4_ERR_LAUNCH;
+  if (!encode_scales_map(&tm_sfa, a.a_scales, a.M, a.K)) return NVFP4_ERR_LAUNCH;
+  if (!encode_scales_map(&tm_sfb, a.b_scales, a.N, a.K)) return NVFP4_ERR_LAUNCH;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -444,12 +555,35 @@ nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   ep.out_fp32 = a.out_fp32;
   const int num_m = static_cast<int>((a.M + kBM - 1) / kBM);
   const int num_n = static_cast<int>((a.N + kBN - 1) / kBN);
-  const int num_tiles = num_m * num_n;
-  const int grid = std::min(num_tiles, sm_count());
-  gemm_nvfp4_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_a, tm_b, a.a_scales, a.b_scales,
-                                                       static_cast<int>(a.K), num_m, num_tiles, ep, a.err,
-                                                       wait_timeout_ns());
-  return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH;
+  const int num_pair_tiles = ((num_m + kCluster - 1) / kCluster) * num_n;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // as many clusters as can be resident at once (pairs are placed within a GPC)
+  static int max_clusters = [&] {
+    int n = 0;
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(sm_count(), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_kernel, &q) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = sm_count() / kCluster;
+    }
+    return n;
+  }();
+  const int clusters = std::max(1, std::min(num_pair_tiles, max_clusters));
+  cfg.gridDim = dim3(clusters * kCluster, 1, 1);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, tm_a, tm_b, tm_sfa, tm_sfb,
+                                           static_cast<int>(a.K), num_m, num_pair_tiles, ep, a.err,
+                                           wait_timeout_ns());
+  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH;
 }
 
 }  // namespace nvfp4

@@ -1,6 +1,7 @@
 // nvfp4_quantize_noalloc: the activation quantizer for callers that cannot allocate device
-// memory (see include/nvfp4.h). Its scratch -- the word the tensor-amax pass reduces into --
-// lives in a fixed array inside this library instead of a caller-provided workspace.
+// memory (see include/nvfp4.h). Its scratch -- the word the tensor-amax pass reduces into
+// and a finished-CTA count -- lives in a fixed array inside this library instead of a
+// caller-provided workspace.
 
 #include <cuda_runtime.h>
 
@@ -56,7 +57,11 @@ nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t K, int64_t
   if (nvfp4_workspace_bytes() > kNoAllocScratchBytes) return NVFP4_ERR_SHAPE;
   void* scratch = nullptr;
   if (nvfp4_status st = scratch_address(&scratch); st != NVFP4_OK) return st;
-  // nvfp4_quantize clears the amax word it needs (an async memset on `stream`) before use.
+  // Start from a zeroed scratch every call (the amax word and the finished-CTA count), so
+  // an earlier call that was interrupted cannot leave this shared array in a bad state.
+  if (cudaMemsetAsync(scratch, 0, nvfp4_workspace_bytes(), reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return NVFP4_ERR_LAUNCH;
   return nvfp4_quantize(x, M, K, ldx, codes, scales, tensor_scale, nullptr, scratch, stream);
 }
 

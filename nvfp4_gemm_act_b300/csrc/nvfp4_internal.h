@@ -20,10 +20,11 @@ int sm_count();
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
                         unsigned* amax_bits, cudaStream_t s);
 
-// Quantize x [M, K] (row stride ldx). ts = *ts_in if ts_in, else amax/2688 from *amax_bits.
+// Quantize x [M, K] (row stride ldx). ts = *ts_in if ts_in, else amax/2688 of x: amax_kernel
+// reduces into ws[0], the quantize kernel reads it and leaves ws[0..1] zeroed again.
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                            uint8_t* scales, const unsigned* amax_bits, const float* ts_in,
-                            float* ts_out, cudaStream_t s);
+                            uint8_t* scales, unsigned* ws, const float* ts_in, float* ts_out,
+                            cudaStream_t s);
 
 // W [K, N] -> packed K-major codes [N, K/2] + tiled scales (scales pre-zeroed by caller).
 cudaError_t launch_pack_weights(const void* w, int64_t K, int64_t N, bool gated,

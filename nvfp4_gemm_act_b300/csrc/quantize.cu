@@ -122,22 +122,54 @@ __global__ void __launch_bounds__(kAmaxThreads)
 }
 
 // ---------------------------------------------------------------------------------------
-// Activation quantizer. Work item = one 512-element chunk of a row; lane l owns the
-// 16-element block c * 32 + l (two 16-byte loads), so a warp reads 1 KB of a row per item
-// and writes 256 contiguous code bytes. Items are visited in reverse order (a grid-stride
-// walk from the end of x), so the data the amax pass read last -- still in L2 -- is
-// quantized first. Rows in [M, Mpad) only write their zero scale bytes.
+// Activation quantizer (after amax_kernel when the tensor scale is dynamic). Work item = one
+// 512-element chunk of a row; lane l owns the 16-element block c * 32 + l (two 16-byte
+// loads), so a warp reads 1 KB of a row per item and writes 256 contiguous code bytes.
+// Items are visited in reverse order (a grid-stride walk from the end of x), so the data
+// the amax pass read last -- still in L2 -- is quantized first. Rows in [M, Mpad) only
+// write their zero scale bytes.
+//
+// Workspace words (zero between calls): ws[0] = amax bits (amax_kernel's atomic max),
+// ws[1] = count of finished CTAs. Every CTA reads ws[0] before it counts itself finished;
+// the last CTA to finish therefore knows all reads are done and zeroes both words.
 // ---------------------------------------------------------------------------------------
 constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;
 
+struct QuantItem {
+  uint32_t row, blk;
+  bool live, real;
+};
+
+__device__ __forceinline__ QuantItem quant_item(uint32_t item, uint32_t lane, uint32_t M,
+                                                uint32_t blocks_per_row, uint32_t chunks_per_row) {
+  QuantItem q;
+  q.row = item / chunks_per_row;
+  q.blk = (item - q.row * chunks_per_row) * 32u + lane;
+  q.live = q.blk < blocks_per_row;
+  q.real = q.live && q.row < M;
+  return q;
+}
+
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M,
                     uint32_t blocks_per_row, uint32_t chunks_per_row, uint32_t total_items,
-                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                    const unsigned* __restrict__ amax_bits, const float* __restrict__ ts_in,
-                    float* __restrict__ ts_out) {
-  const float ts = ts_in != nullptr ? *ts_in : __fdiv_rn(__uint_as_float(*amax_bits), kTsDivisor);
+                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, unsigned* ws,
+                    const float* __restrict__ ts_in, float* __restrict__ ts_out) {
+  float ts;
+  if (ts_in != nullptr) {
+    ts = *ts_in;
+  } else {
+    ts = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile unsigned*>(ws)), kTsDivisor);
+    __syncthreads();  // every thread of this CTA has read the amax word
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(ws + 1, 1u) == gridDim.x - 1u) {  // last CTA: all CTAs have read it
+        ws[0] = 0u;
+        ws[1] = 0u;
+      }
+    }
+  }
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
   const float six_ts = __fmul_rn(6.0f, ts);
   const uint32_t lane = threadIdx.x & 31u;
@@ -148,36 +180,33 @@ __global__ void __launch_bounds__(kQuantThreads)
 
   for (uint32_t base = warp; base < total_items; base += nwarps * kQuantUnroll) {
     uint4 lo[kQuantUnroll], hi[kQuantUnroll];
-    uint32_t row[kQuantUnroll], blk[kQuantUnroll];
-    bool live[kQuantUnroll], real[kQuantUnroll];
+    QuantItem q[kQuantUnroll];
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t i = base + u * nwarps;                  // walk order
+      const uint32_t i = base + u * nwarps;
       const bool in = i < total_items;
-      const uint32_t item = in ? total_items - 1u - i : 0u;  // reversed
-      row[u] = item / chunks_per_row;
-      blk[u] = (item - row[u] * chunks_per_row) * 32u + lane;
-      live[u] = in && blk[u] < blocks_per_row;
-      real[u] = live[u] && row[u] < M;
+      q[u] = quant_item(in ? total_items - 1u - i : 0u, lane, M, blocks_per_row, chunks_per_row);
+      q[u].live = q[u].live && in;
+      q[u].real = q[u].real && in;
       lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (real[u]) {
-        const __nv_bfloat16* src = x + row[u] * ldx + blk[u] * 16u;
+      if (q[u].real) {
+        const __nv_bfloat16* src = x + q[u].row * ldx + q[u].blk * 16u;
         lo[u] = ld_nc_v4(src);
         hi[u] = ld_nc_v4(src + 8);
       }
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      if (!live[u]) continue;
+      if (!q[u].live) continue;
       uint32_t scale = 0u;
-      if (real[u]) {
+      if (q[u].real) {
         const BlockScale bs = block_scale(fmaxf(absmax8(lo[u]), absmax8(hi[u])), ts, six_ts);
-        uint2 q = make_uint2(0u, 0u);
-        if (bs.live) q = make_uint2(encode8(lo[u], bs.inv), encode8(hi[u], bs.inv));
-        *reinterpret_cast<uint2*>(codes + row[u] * row_code_bytes + blk[u] * 8u) = q;
+        uint2 c = make_uint2(0u, 0u);
+        if (bs.live) c = make_uint2(encode8(lo[u], bs.inv), encode8(hi[u], bs.inv));
+        *reinterpret_cast<uint2*>(codes + q[u].row * row_code_bytes + q[u].blk * 8u) = c;
         scale = bs.code;
       }
-      const uint32_t r = row[u], b = blk[u];
+      const uint32_t r = q[u].row, b = q[u].blk;
       scales[((r >> 7) * gpr + (b >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (b & 3u)] =
           static_cast<uint8_t>(scale);
     }
@@ -276,8 +305,12 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
 }
 
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
-                            uint8_t* scales, const unsigned* amax_bits, const float* ts_in,
-                            float* ts_out, cudaStream_t s) {
+                            uint8_t* scales, unsigned* ws, const float* ts_in, float* ts_out,
+                            cudaStream_t s) {
+  if (ts_in == nullptr) {
+    const cudaError_t e = launch_amax(x, M, K, ldx, ws, s);
+    if (e != cudaSuccess) return e;
+  }
   const uint32_t bpr = static_cast<uint32_t>(K / 16);
   const uint32_t cpr = (bpr + 31u) / 32u;
   const int64_t mpad = (M + 127) / 128 * 128;
@@ -287,9 +320,8 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   const uint32_t want = (total + items_per_block - 1) / items_per_block;
   const uint32_t grid = std::max<uint32_t>(1u, std::min<uint32_t>(want, (uint32_t)(sm_count() * per_sm)));
   quantize_kernel<<<grid, kQuantThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
-                                                 static_cast<uint64_t>(ldx),
-                                                 static_cast<uint32_t>(M), bpr, cpr, total, codes,
-                                                 scales, amax_bits, ts_in, ts_out);
+                                                 static_cast<uint64_t>(ldx), static_cast<uint32_t>(M),
+                                                 bpr, cpr, total, codes, scales, ws, ts_in, ts_out);
   return cudaGetLastError();
 }
 

@@ -140,3 +140,22 @@ def test_pack_gated_up_full_size_sampled_rows():
                                      np.random.default_rng(8).integers(0, w.N, 56)]))
     rc, rs, _ = R.quantize_ref(np.ascontiguousarray(wn.T[perm[rows]]), ts)
     assert_quant_equal((gc[rows], gs[rows], gt), (rc, rs, ts), "gated W sampled")
+
+
+def test_workspace_reused_across_calls():
+    # one zeroed workspace, reused: amax going down, up, down again, with a static-scale call
+    # and a weight pack on the same workspace in between; every call matches the oracle
+    ws = torch.zeros(nv.nvfp4_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    rng = np.random.default_rng(21)
+    scales = [50.0, 0.5, 7.0, 1e-3, 3.0]
+    for i, s in enumerate(scales):
+        x = _bf16(rng.standard_normal((130, 512)) * s)
+        q = nv.nvfp4_quantize(x.to(DEV), workspace=ws)
+        assert_quant_equal(gpu_nvfp4_to_np(q), R.quantize_ref(to_np_f32(x)), f"call {i}")
+        if i == 1:
+            tsi = torch.tensor([0.01], dtype=torch.float32, device=DEV)
+            q = nv.nvfp4_quantize(x.to(DEV), tensor_scale_in=tsi, workspace=ws)
+            assert_quant_equal(gpu_nvfp4_to_np(q), R.quantize_ref(to_np_f32(x), np.float32(0.01)), "static")
+        if i == 2:
+            w = _bf16(rng.standard_normal((128, 64)) * 100.0)
+            nv.nvfp4_pack_weights(w.to(DEV), workspace=ws)
