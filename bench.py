@@ -199,9 +199,13 @@ class ClockSampler:
 # The GPU arm
 # ---------------------------------------------------------------------------------------
 
-def kernel_source_hash() -> str:
+KERNEL_SOURCES = {"gemm": ("gemm.cu", "nvfp4_device.cuh"), "quantize": ("quantize.cu", "nvfp4_device.cuh")}
+
+
+def kernel_source_hash(op: str) -> str:
+    """Hash of the CUDA sources that build `op`'s kernels ("gemm_*" or "quantize_*")."""
     h = hashlib.sha256()
-    for f in ("gemm.cu", "quantize.cu", "nvfp4_device.cuh"):
+    for f in KERNEL_SOURCES["gemm" if op.startswith("gemm") else "quantize"]:
         with open(os.path.join(ROOT, "nvfp4_gemm_act_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -213,7 +217,7 @@ def read_traffic(op: str):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(op)
     for line in open(path):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == op and parts[1] == src:

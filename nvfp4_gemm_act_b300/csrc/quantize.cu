@@ -29,6 +29,13 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return v;
 }
 
+// 32 bytes in one 256-bit load (address 32-byte aligned).
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint4& lo, uint4& hi) {
+  asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+               : "l"(p));
+}
+
 // |bf16| maximum of the 8 values in v, as the fp32 value (exact).
 __device__ __forceinline__ float absmax8(const uint4& v) {
   uint32_t m = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
@@ -151,6 +158,7 @@ __device__ __forceinline__ QuantItem quant_item(uint32_t item, uint32_t lane, ui
   return q;
 }
 
+template <bool kLoad32>  // one 32-byte load per lane (x 32-byte aligned, ldx % 16 == 0)
 __global__ void __launch_bounds__(kQuantThreads)
     quantize_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M,
                     uint32_t blocks_per_row, uint32_t chunks_per_row, uint32_t total_items,
@@ -191,8 +199,12 @@ __global__ void __launch_bounds__(kQuantThreads)
       lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
       if (q[u].real) {
         const __nv_bfloat16* src = x + q[u].row * ldx + q[u].blk * 16u;
-        lo[u] = ld_nc_v4(src);
-        hi[u] = ld_nc_v4(src + 8);
+        if (kLoad32) {
+          ld_nc_v8(src, lo[u], hi[u]);
+        } else {
+          lo[u] = ld_nc_v4(src);
+          hi[u] = ld_nc_v4(src + 8);
+        }
       }
     }
 #pragma unroll
@@ -315,13 +327,15 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
   const uint32_t cpr = (bpr + 31u) / 32u;
   const int64_t mpad = (M + 127) / 128 * 128;
   const uint32_t total = static_cast<uint32_t>(mpad * cpr);
-  static const int per_sm = resident_blocks((const void*)quantize_kernel, kQuantThreads, 0);
+  static const int per_sm = resident_blocks((const void*)quantize_kernel<true>, kQuantThreads, 0);
   const uint32_t items_per_block = (kQuantThreads / 32) * kQuantUnroll;
   const uint32_t want = (total + items_per_block - 1) / items_per_block;
   const uint32_t grid = std::max<uint32_t>(1u, std::min<uint32_t>(want, (uint32_t)(sm_count() * per_sm)));
-  quantize_kernel<<<grid, kQuantThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
-                                                 static_cast<uint64_t>(ldx), static_cast<uint32_t>(M),
-                                                 bpr, cpr, total, codes, scales, ws, ts_in, ts_out);
+  const bool load32 = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ldx % 16 == 0;
+  auto kern = load32 ? quantize_kernel<true> : quantize_kernel<false>;
+  kern<<<grid, kQuantThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x), static_cast<uint64_t>(ldx),
+                                      static_cast<uint32_t>(M), bpr, cpr, total, codes, scales, ws, ts_in,
+                                      ts_out);
   return cudaGetLastError();
 }
 

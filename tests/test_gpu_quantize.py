@@ -159,3 +159,14 @@ def test_workspace_reused_across_calls():
         if i == 2:
             w = _bf16(rng.standard_normal((128, 64)) * 100.0)
             nv.nvfp4_pack_weights(w.to(DEV), workspace=ws)
+
+
+def test_rows_only_16_byte_aligned():
+    # x starting 16 bytes into an allocation: the kernel must use 16-byte loads
+    x = W.make_x(W.QKV_RMSNORM.with_m(64))
+    big = torch.zeros(64, 3072 + 8, dtype=torch.bfloat16)
+    big[:, 8:] = x
+    view = big.to(DEV)[:, 8:]
+    assert view.data_ptr() % 32 == 16
+    q = nv.nvfp4_quantize(view)
+    assert_quant_equal(gpu_nvfp4_to_np(q), R.quantize_ref(to_np_f32(x)), "16-byte aligned rows")
