@@ -50,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-rows", type=int, default=16, help="oracle rows sampled per GEMM")
     p.add_argument("--only", choices=["qkv_rmsnorm", "gated_up", "down_bias"], default=None,
                    help="run one of the three layers only (for profiler captures)")
+    p.add_argument("--sweep", action="store_true",
+                   help="batch sweep: one JSON line per (M, GEMM), M in 512..18432")
     return p.parse_args(argv)
 
 
@@ -378,38 +380,69 @@ def run_ours(args, world, rank, local):
 
 
 def run_e2e(args, layers, dev, dist):
-    """Same metric through the C ABI with host inputs and outputs: every step copies the
-    three activations from pinned host memory and the three outputs back."""
+    """Same metric through the public API with host inputs and outputs: every step copies the
+    three activations from pinned host memory and the three outputs back to pinned host
+    memory. Copies run on their own streams (host->device, device->host: PCIe is full
+    duplex) and device buffers are double-buffered, so step k+1's inputs stream in and step
+    k's outputs stream out while kernels run, as a serving loop would pipeline it."""
     import torch
+
+    import nvfp4_gemm_act_b300 as nv
     hx = [l.x.cpu().pin_memory() for l in layers]
-    hy = [torch.empty(l.out.shape, dtype=l.out.dtype, pin_memory=True) for l in layers]
+    hy = [[torch.empty(l.out.shape, dtype=l.out.dtype, pin_memory=True) for l in layers] for _ in range(2)]
+    dx = [[torch.empty_like(l.x) for l in layers] for _ in range(2)]
+    dy = [[torch.empty_like(l.out) for l in layers] for _ in range(2)]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    x_free = [ev(), ev()]   # compute finished reading dx[b]
+    x_ready = [ev(), ev()]  # dx[b] copied in
+    y_ready = [ev(), ev()]  # dy[b] written
+    y_free = [ev(), ev()]   # dy[b] copied out
+    for b in range(2):
+        for e_ in (x_free[b], y_free[b]):
+            e_.record(s_comp)
     flops = sum(l.w.flops for l in layers)
 
-    def step():
-        for l, h in zip(layers, hx):
-            l.x.copy_(h, non_blocking=True)
-        for l in layers:
-            l.quantize()
-            l.gemm()
-        for l, h in zip(layers, hy):
-            h.copy_(l.out, non_blocking=True)
+    def step(k):
+        b = k % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(x_free[b])
+            for d, h in zip(dx[b], hx):
+                d.copy_(h, non_blocking=True)
+            x_ready[b].record(s_in)
+        s_comp.wait_event(x_ready[b])
+        s_comp.wait_event(y_free[b])
+        for l, xin, yout in zip(layers, dx[b], dy[b]):
+            w = l.w
+            nv.nvfp4_quantize(xin, out=l.qa, workspace=l.ws, stream=s_comp)
+            nv.nvfp4_gemm(l.qa, l.qb, w.epilogue, bias=l.bias, gamma=l.gamma, head_dim=w.head_dim,
+                          norm_cols=w.norm_cols, eps=w.eps, out=yout, device_error=l.err, stream=s_comp)
+        x_free[b].record(s_comp)
+        y_ready[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(y_ready[b])
+            for h, d in zip(hy[b], dy[b]):
+                h.copy_(d, non_blocking=True)
+            y_free[b].record(s_out)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
+    for k in range(max(args.warmup, 3)):
+        step(k)
     torch.cuda.synchronize()
     K = max(3, min(args.steps, 20))
     barrier(dist)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(K):
-        step()
+    for k in range(K):
+        step(k)
     torch.cuda.synchronize()
     el = time.perf_counter() - t0
+    for l in layers:
+        assert nv.nvfp4_get_device_error(l.err) == 0
     t_max, units = aggregate(el, flops * K, dist)
     return {"value": round(units / t_max / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(sum(h.numel() * h.element_size() for h in hx)),
-            "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for h in hy)),
-            "steps": K}
+            "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for h in hy[0])),
+            "steps": K, "pipelined": "H2D / compute / D2H streams, double-buffered"}
 
 
 # ---------------------------------------------------------------------------------------
@@ -500,9 +533,60 @@ def run_reference(args, world, rank):
     print(json.dumps(res), flush=True)
 
 
+def run_sweep(args):
+    """The three DiT GEMMs at every batch size of the sweep (activations redrawn per size,
+    weights fixed): CUDA-event time of the activation quantize and of the fused GEMM, L2
+    flushed before each timed call; one JSON line per (M, GEMM)."""
+    import torch
+
+    import nvfp4_gemm_act_b300 as nv
+    from nvfp4_gemm_act_b300 import workloads as W
+    dev = "cuda:0"
+    peaks, _ = measured_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    packed = {}
+    for w in W.sweep_workloads():
+        base = w.name.rsplit("_m", 1)[0]
+        if base not in packed:
+            packed[base] = nv.nvfp4_pack_weights(W.make_w(w).to(dev), gated_interleave=w.epilogue == "gated_silu")
+        l = Layer.__new__(Layer)
+        l.w, l.x, l.qb = w, W.make_x(w).to(dev), packed[base]
+        b, g = W.make_bias(w), W.make_gamma(w)
+        l.bias = None if b is None else b.to(dev)
+        l.gamma = None if g is None else g.to(dev)
+        l.qa = nv._alloc_nvfp4(w.M, w.K, dev)
+        l.ws = torch.zeros(16, dtype=torch.uint8, device=dev)
+        l.out = torch.empty((w.M, w.out_cols), dtype=torch.bfloat16, device=dev)
+        l.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        times = {"quantize": [], "gemm": []}
+        for it in range(max(args.warmup, 3) + args.steps):
+            for name, fn in (("quantize", l.quantize), ("gemm", l.gemm)):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                if it >= max(args.warmup, 3):
+                    times[name].append(e0.elapsed_time(e1))
+        assert nv.nvfp4_get_device_error(l.err) == 0
+        qms, gms = float(np.median(times["quantize"])), float(np.median(times["gemm"]))
+        qbytes = w.M * w.K * 2 + w.M * w.K // 2 + w.M * w.K // 16
+        tf = w.flops / (gms / 1e3) / 1e12
+        print(json.dumps({"sweep": w.name, "M": w.M, "epilogue": w.epilogue, "gemm_ms": round(gms, 5),
+                          "gemm_tflops": round(tf, 1), "frac_of_measured_fp4": round(tf / fp4_peak, 4),
+                          "frac_of_15pf": round(tf / (NOMINAL_FP4_PF * 1e3), 4),
+                          "quantize_ms": round(qms, 5),
+                          "quantize_gbs": round(qbytes / (qms / 1e3) / 1e9, 1)}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:

@@ -17,7 +17,8 @@ Shapes follow a FLUX-class DiT block (hidden 3072, MLP 12288, 12 heads x head_di
                   bias N(0, 0.01)
 
 Every array is drawn in fp64 from ``numpy.random.default_rng((seed, stream))`` (stream 0:
-X, 1: W, 2: bias, 3: gamma, 4: outlier channels) and rounded to bf16 (X, W) or fp32
+X, 1: W, 2: bias, 3: gamma, 4: outlier channels; all but X use the layer's seed,
+which ``with_m`` keeps when it reseeds the activations) and rounded to bf16 (X, W) or fp32
 (bias, gamma) by torch's round-to-nearest-even conversion.
 """
 from __future__ import annotations
@@ -46,6 +47,7 @@ class Workload:
     norm_cols: int = 0
     eps: float = 1e-6
     gamma_std: float = 0.1
+    w_seed: Optional[int] = None  # weights / bias / gamma seed; None = `seed`
 
     @property
     def out_cols(self) -> int:
@@ -55,9 +57,14 @@ class Workload:
     def flops(self) -> int:
         return 2 * self.M * self.N * self.K
 
+    @property
+    def layer_seed(self) -> int:
+        return self.seed if self.w_seed is None else self.w_seed
+
     def with_m(self, M: int, seed: Optional[int] = None) -> "Workload":
+        """The same layer (weights, bias, gamma) on M tokens; `seed` reseeds the activations."""
         return dataclasses.replace(self, M=M, seed=self.seed if seed is None else seed,
-                                   name=f"{self.name}_m{M}")
+                                   w_seed=self.layer_seed, name=f"{self.name}_m{M}")
 
 
 TINY_BIAS = Workload("tiny_bias", 128, 256, 256, EPI_BIAS, seed=0)
@@ -68,7 +75,8 @@ DOWN_BIAS = Workload("down_bias", 4608, 12288, 3072, EPI_BIAS, seed=4, x_dist="s
 
 WORKLOADS = {w.name: w for w in (TINY_BIAS, QKV_RMSNORM, GATED_UP, DOWN_BIAS)}
 
-# Batch sweep: the three DiT GEMMs at M in {512, 1024, 4608, 9216, 18432}, seeds 10..14.
+# Batch sweep: the three DiT GEMMs at M in {512, 1024, 4608, 9216, 18432}; activations of
+# the i-th size drawn with seed 10 + i, each layer keeping its weights.
 SWEEP_M = (512, 1024, 4608, 9216, 18432)
 
 
@@ -101,26 +109,26 @@ def make_x(w: Workload, rows: Optional[int] = None) -> torch.Tensor:
         raise ValueError(w.x_dist)
     if w.x_dist == "normal_outliers":
         n_out = int(round(0.01 * w.K))
-        ch = _rng(w.seed, 4).choice(w.K, n_out, replace=False)
+        ch = _rng(w.layer_seed, 4).choice(w.K, n_out, replace=False)  # a property of the layer input
         x[:, ch] *= 20.0
     return _bf16(x)
 
 
 def make_w(w: Workload) -> torch.Tensor:
     """Weights W [K, N] (row-major, as a linear layer's x @ W) as a CPU bf16 tensor."""
-    return _bf16(w.w_std * _rng(w.seed, 1).standard_normal((w.K, w.N)))
+    return _bf16(w.w_std * _rng(w.layer_seed, 1).standard_normal((w.K, w.N)))
 
 
 def make_bias(w: Workload) -> Optional[torch.Tensor]:
     """fp32 bias indexed by original output column ([N]), or None."""
     if w.bias_std is None:
         return None
-    return torch.from_numpy((w.bias_std * _rng(w.seed, 2).standard_normal(w.N)).astype(np.float32))
+    return torch.from_numpy((w.bias_std * _rng(w.layer_seed, 2).standard_normal(w.N)).astype(np.float32))
 
 
 def make_gamma(w: Workload) -> Optional[torch.Tensor]:
     """fp32 RMSNorm gain, one value per normalised column ([norm_cols]), or None."""
     if w.epilogue != EPI_HEAD_RMSNORM:
         return None
-    g = 1.0 + w.gamma_std * _rng(w.seed, 3).standard_normal(w.norm_cols)
+    g = 1.0 + w.gamma_std * _rng(w.layer_seed, 3).standard_normal(w.norm_cols)
     return torch.from_numpy(g.astype(np.float32))
