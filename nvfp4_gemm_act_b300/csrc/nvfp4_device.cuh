@@ -149,9 +149,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 }
 
 // Arrive on an mbarrier given by its shared::cluster address (possibly in another CTA).
+// Arrive on a barrier of any CTA of the cluster, with CTA-scope release semantics: it orders
+// nothing but this thread's own prior work, so it does not wait for this thread's earlier
+// global stores to become visible cluster-wide (a cluster-scope release would). Callers that
+// hand TMEM back to the MMA thread order their tcgen05.ld first with tcgen05.wait::ld and
+// tcgen05.fence::before_thread_sync.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
 
 // 1-D bulk copy: dst, src 16-byte aligned, bytes % 16 == 0.
