@@ -88,9 +88,10 @@ NVFP4_API int64_t nvfp4_scale_offset(int64_t row, int64_t kblock, int64_t K);
 
 /* Bytes of scratch `workspace` that nvfp4_quantize / nvfp4_pack_weights need (16).
  * nvfp4_quantize expects the workspace zero-filled before its first use and leaves it
- * zero-filled again (its amax word and a finished-CTA count), so allocate and zero it once
- * and reuse it; nvfp4_pack_weights also leaves it zero-filled. Calls that use the same
- * workspace must not overlap on the GPU. */
+ * zero-filled again (its amax word and CTA counters), so allocate and zero it once and
+ * reuse it; nvfp4_pack_weights also leaves it zero-filled. Calls that use the same
+ * workspace must not overlap on the GPU. After a call that reported a device-side time-out
+ * (a NaN tensor_scale, see nvfp4_quantize) zero it again before reuse. */
 NVFP4_API size_t nvfp4_workspace_bytes(void);
 
 /*
@@ -107,8 +108,16 @@ NVFP4_API size_t nvfp4_workspace_bytes(void);
  *   workspace  >= nvfp4_workspace_bytes() device bytes, 16-byte aligned, zero-filled
  *            before its first use and then reused (see nvfp4_workspace_bytes); may be NULL
  *            when tensor_scale_in is given.
- * Two launches: an amax pass over x (skipped for a static scale), then the quantize pass,
- * which walks x backwards so that what the amax pass read last is still in L2.
+ * Dynamic scale, x small enough to sit in the shared memory of all SMs (each CTA's rows
+ * within 200 KB: M * K up to about 14.8M elements) and 16-byte aligned rows: one cooperative
+ * launch reads x once into shared memory, reduces the amax, meets the other CTAs at a
+ * grid-wide barrier on the workspace words and quantizes. Otherwise two launches: an amax
+ * pass over x (skipped for a static scale), then the quantize pass, which walks x backwards
+ * so that what the amax pass read last is still in L2. Codes and scales are identical
+ * either way.
+ * If a device-side wait of the single launch runs out of time (NVFP4_WAIT_TIMEOUT_NS,
+ * default 2 s; it cannot under a cooperative launch unless the GPU misbehaves), tensor_scale
+ * is written NaN, no codes are written, and the workspace must be zeroed before reuse.
  * Per block of 16: s = E4M3(bamax / fp32(6 ts)) (nearest even, saturating at 448);
  * d = fp32(dec(s) ts); if d < 2^-126 the block stores scale 0 and codes +0; otherwise each
  * element is coded E2M1(fp32(x * fp32(1/d))) (nearest even, saturating at 6; a negative

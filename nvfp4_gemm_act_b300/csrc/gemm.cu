@@ -14,9 +14,9 @@
 // (row-tile pair, weight tile) tiles round-robin, row pairs fastest, so concurrent pairs
 // share weight tiles in L2.
 //   warp 0     (both CTAs) TMA producer: this CTA's A tile, its half of the B tile, its A
-//              scale tile and both B scale bands (every CTA needs the scales of all 256
-//              columns in its TMEM); all of them complete on the leader CTA's full barrier;
-//              L2 prefetch 8 k-blocks ahead;
+//              scale tile, and one of the two B scale bands multicast to both CTAs (every
+//              CTA needs the scales of all 256 columns in its TMEM); all of them complete on
+//              the leader CTA's full barrier; L2 prefetch 8 k-blocks ahead;
 //   warp 1     (both CTAs) TMEM allocation (pair-collective); in the leader, the single
 //              MMA-issuing thread, whose commits release the stage and publish the
 //              accumulator in both CTAs;
@@ -83,6 +83,7 @@ constexpr int kXchBytes = 2 * kBM * 4;
 constexpr int kOffEpiBuf = kOffXch + kXchBytes;               // per-warp store staging
 constexpr int kEpiBufBytes = 32 * 64;                         // 32 rows x 64 bytes per warp
 constexpr int kOffFlags = kOffEpiBuf + kEpiWarps * kEpiBufBytes;  // epilogue wait results
+static_assert(2 * kEpiWarps * 4 <= 64, "two tiles' epilogue flags");
 constexpr int kOffBar = kOffFlags + 64;
 constexpr int kBarBytes = 256;
 constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;        // + slack to align to 1 KB
@@ -327,9 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // scale tiles: row = band * k_atoms + first k-atom of the stage (4 atoms of 512 B)
           tma_load_2d_pair(sbase + kOffSfa + s * kSfaBytes, &tm_sfa, 0,
                            m_blk * k_atoms + kb * kKStepsPerStage, bar, pol);
-          for (int h = 0; h < kBN / 128; ++h)
-            tma_load_2d_pair(sbase + kOffSfb + s * kSfbBytes + h * (kSfbBytes / 2), &tm_sfb, 0,
-                             (n_blk * 2 + h) * k_atoms + kb * kKStepsPerStage, bar, pol);
+          // B scale band `rank` of the tile, multicast to both CTAs (each needs both bands)
+          tma_load_2d_pair_mc(sbase + kOffSfb + s * kSfbBytes + rank * (kSfbBytes / 2), &tm_sfb, 0,
+                              (n_blk * 2 + rank) * k_atoms + kb * kKStepsPerStage, bar, 0x3, pol);
           ++kc;
         }
       }
@@ -444,13 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         bias_s[et] = b;
         gamma_s[et] = g;
       }
+      // Each warp pulls its columns as soon as it sees the accumulator and hands TMEM back
+      // to the leader's MMA warp; the epilogue-wide barrier (parameters staged, every warp's
+      // wait result known) comes after, off the MMA warp's critical path.
+      // (After a timed-out wait the pull reads stale TMEM, which is harmless: nothing is
+      // stored and TMEM is not handed back.)
       const bool ready = __all_sync(0xFFFFFFFFu, mbar_wait(acc_full_bar, it & 1u, timeout_ns, err));
-      if (lane == 0) flags[ew] = ready ? 1 : 0;
-      named_bar_sync(kBarEpiParams, kEpiThreads);
-      bool all_ready = true;
-#pragma unroll
-      for (int w = 0; w < kEpiWarps; ++w) all_ready = all_ready && flags[w] != 0;
-      if (!all_ready) break;  // uniform across the epilogue warps
       tc_fence_after();
       float z[kHalf];
       {
@@ -462,10 +462,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32cols(taddr + 96, *reinterpret_cast<uint32_t(*)[32]>(r + 96));
         tmem_ld_wait();
       }
-      // accumulator is in registers: tell the leader's MMA warp this TMEM is free
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_acc_empty);
+      if (ready && lane == 0) mbar_arrive_cluster(leader_acc_empty);
+      // flags double-buffered by tile parity: a warp that is already on the next tile never
+      // overwrites a flag another warp has still to read for this one
+      volatile int* tile_flags = flags + (it & 1u) * kEpiWarps;
+      if (lane == 0) tile_flags[ew] = ready ? 1 : 0;
+      named_bar_sync(kBarEpiParams, kEpiThreads);
+      bool all_ready = true;
+#pragma unroll
+      for (int w = 0; w < kEpiWarps; ++w) all_ready = all_ready && tile_flags[w] != 0;
+      if (!all_ready) break;  // uniform across the epilogue warps
       const float* bh = bias_s + half * kHalf;
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) z[i] = fmaf(alpha, z[i], bh[i]);

@@ -20,8 +20,9 @@ int sm_count();
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
                         unsigned* amax_bits, cudaStream_t s);
 
-// Quantize x [M, K] (row stride ldx). ts = *ts_in if ts_in, else amax/2688 of x: amax_kernel
-// reduces into ws[0], the quantize kernel reads it and leaves ws[0..1] zeroed again.
+// Quantize x [M, K] (row stride ldx). ts = *ts_in if ts_in, else amax/2688 of x: either one
+// cooperative single-pass launch (x fits in the SMs' shared memory) or amax_kernel reducing
+// into ws[0] and the quantize kernel reading it; both leave ws[0..3] zeroed again.
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                             uint8_t* scales, unsigned* ws, const float* ts_in, float* ts_out,
                             cudaStream_t s);

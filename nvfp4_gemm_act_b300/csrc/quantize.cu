@@ -3,8 +3,8 @@
 //
 // Format (page "How fal made Ideogram V4 6x faster", NVFP4 paragraph): E2M1 codes, one
 // unsigned E4M3 scale per 16 contiguous K-elements, fp32 tensor scale ts = amax / (6 * 448).
-// Per block: s = E4M3(bamax / fp32(6 ts)); d = fp32(dec(s) ts); a block with d < 2^-126 is
-// stored as scale 0 / codes +0; otherwise code = E2M1(fp32(x * fp32(1 / d))).
+// Per block: s = E4M3(fp32(bamax / fp32(6 ts))); d = fp32(dec(s) ts); a block with
+// d < 2^-126 is stored as scale 0 / codes +0; otherwise code = E2M1(fp32(x * fp32(1 / d))).
 // All roundings are IEEE round-to-nearest-even in fp32 (explicit __fmul_rn / __fdiv_rn and
 // the saturating cvt instructions), so codes and scales are reproducible bit for bit.
 
@@ -34,14 +34,6 @@ __device__ __forceinline__ void ld_nc_v8(const void* p, uint4& lo, uint4& hi) {
   asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
                : "l"(p));
-}
-
-// |bf16| maximum of the 8 values in v, as the fp32 value (exact).
-__device__ __forceinline__ float absmax8(const uint4& v) {
-  uint32_t m = __vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
-  m = __vmaxu2(m, __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-  const uint32_t hi = max(m & 0xFFFFu, m >> 16);
-  return __uint_as_float(hi << 16);
 }
 
 struct BlockScale {
@@ -130,11 +122,20 @@ __global__ void __launch_bounds__(kAmaxThreads)
 
 // ---------------------------------------------------------------------------------------
 // Activation quantizer (after amax_kernel when the tensor scale is dynamic). Work item = one
-// 512-element chunk of a row; lane l owns the 16-element block c * 32 + l (two 16-byte
-// loads), so a warp reads 1 KB of a row per item and writes 256 contiguous code bytes.
-// Items are visited in reverse order (a grid-stride walk from the end of x), so the data
-// the amax pass read last -- still in L2 -- is quantized first. Rows in [M, Mpad) only
+// 512-element chunk of a row; lane l owns the 16-element block c * 32 + l (one 32-byte or
+// two 16-byte loads), so a warp reads 1 KB of a row per item and writes 256 contiguous code
+// bytes. Items are visited in reverse order (a grid-stride walk from the end of x), so the
+// data the amax pass read last -- still in L2 -- is quantized first. Rows in [M, Mpad) only
 // write their zero scale bytes.
+//
+// Per block, without a division in the common case:
+//  * scale code s = E4M3(fp32(bamax / fp32(6 ts))): the quotient is approximated as
+//    bamax * fp32(1 / (6 ts)) (within 2 ulp of the rounded quotient) and rounded to E4M3 at
+//    both ends of a +-2^-20 relative window; when the two ends disagree the quotient is
+//    within a few ulp of an E4M3 rounding boundary and the exact IEEE division decides, so
+//    s always equals the code of the correctly rounded quotient;
+//  * fp32(1 / d) with d = fp32(dec(s) ts) takes one of 127 values for the whole tensor: each
+//    CTA tabulates them in shared memory (with the stored code, 0 for a zero block).
 //
 // Workspace words (zero between calls): ws[0] = amax bits (amax_kernel's atomic max),
 // ws[1] = count of finished CTAs. Every CTA reads ws[0] before it counts itself finished;
@@ -143,62 +144,120 @@ __global__ void __launch_bounds__(kAmaxThreads)
 constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;
 
-struct QuantItem {
-  uint32_t row, blk;
-  bool live, real;
+// max(|a|, |b|) per bf16 lane (the sign of the result is discarded by the caller).
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// |bf16| maximum of the 16 values in lo, hi, as the fp32 value (exact).
+__device__ __forceinline__ float absmax16(const uint4& lo, const uint4& hi) {
+  const uint32_t m = bf16x2_max_abs(bf16x2_max_abs(bf16x2_max_abs(lo.x, lo.y), bf16x2_max_abs(lo.z, lo.w)),
+                                    bf16x2_max_abs(bf16x2_max_abs(hi.x, hi.y), bf16x2_max_abs(hi.z, hi.w)));
+  const uint32_t h = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
+  return __uint_as_float(h << 16);
+}
+
+// Tables of one tensor scale, built by threads 0..127 (caller synchronises): fp32(1 / d) and
+// the stored code for each E4M3 code s, d = fp32(dec(s) ts); zero entries for a zero block.
+// Code 127 is E4M3 NaN (never produced by the saturating conversion).
+__device__ __forceinline__ void build_scale_tables(float ts, float* inv_tab, uint32_t* code_tab) {
+  if (threadIdx.x < 128) {
+    const uint32_t c = threadIdx.x;
+    const float d = __fmul_rn(e4m3_to_f32(c), ts);
+    const bool live = ts > 0.0f && c < 127u && d >= kFltMin;
+    inv_tab[c] = live ? __fdiv_rn(1.0f, d) : 0.0f;
+    code_tab[c] = live ? c : 0u;
+  }
+}
+
+struct ScaleRoute {
+  float six_ts;
+  float rcp_six_ts;
+  bool fast;  // 1 / (6 ts) finite and normal: the reciprocal route applies
 };
 
-__device__ __forceinline__ QuantItem quant_item(uint32_t item, uint32_t lane, uint32_t M,
-                                                uint32_t blocks_per_row, uint32_t chunks_per_row) {
-  QuantItem q;
-  q.row = item / chunks_per_row;
-  q.blk = (item - q.row * chunks_per_row) * 32u + lane;
-  q.live = q.blk < blocks_per_row;
-  q.real = q.live && q.row < M;
-  return q;
+__device__ __forceinline__ ScaleRoute scale_route(float ts) {
+  ScaleRoute r;
+  r.six_ts = __fmul_rn(6.0f, ts);
+  r.fast = r.six_ts >= 0x1p-125f && r.six_ts <= 0x1p125f;
+  r.rcp_six_ts = r.fast ? __frcp_rn(r.six_ts) : 0.0f;
+  return r;
+}
+
+// One 16-element block (lo: elements 0-7, hi: 8-15): its 8 code bytes; returns the stored
+// scale code (0 for a zero block, whose codes are +0).
+__device__ __forceinline__ uint32_t quantize_block(const uint4& lo, const uint4& hi, const ScaleRoute& sr,
+                                                   const float* inv_tab, const uint32_t* code_tab, uint2& out) {
+  const float bamax = absmax16(lo, hi);
+  uint32_t s;
+  if (sr.fast) {
+    const float qa = __fmul_rn(bamax, sr.rcp_six_ts);
+    const uint32_t s_lo = cvt_e4m3(__fmul_rn(qa, 1.0f - 0x1p-20f));
+    const uint32_t s_hi = cvt_e4m3(__fmul_rn(qa, 1.0f + 0x1p-20f));
+    s = s_lo == s_hi ? s_lo : cvt_e4m3(__fdiv_rn(bamax, sr.six_ts));
+  } else {
+    s = cvt_e4m3(__fdiv_rn(bamax, sr.six_ts));
+  }
+  s &= 127u;
+  const uint32_t stored = code_tab[s];
+  out = make_uint2(0u, 0u);
+  if (stored != 0u) {
+    const float inv = inv_tab[s];
+    out = make_uint2(encode8(lo, inv), encode8(hi, inv));
+  }
+  return stored;
+}
+
+// Byte offset of the scale of (row r, 16-element block kb) in the tiled scale layout.
+__device__ __forceinline__ uint32_t scale_offset(uint32_t r, uint32_t kb, uint32_t gpr) {
+  return ((r >> 7) * gpr + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (kb & 3u);
 }
 
 template <bool kLoad32>  // one 32-byte load per lane (x 32-byte aligned, ldx % 16 == 0)
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kQuantThreads, 4)
     quantize_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M,
                     uint32_t blocks_per_row, uint32_t chunks_per_row, uint32_t total_items,
                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, unsigned* ws,
                     const float* __restrict__ ts_in, float* __restrict__ ts_out) {
-  float ts;
-  if (ts_in != nullptr) {
-    ts = *ts_in;
-  } else {
-    ts = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile unsigned*>(ws)), kTsDivisor);
-    __syncthreads();  // every thread of this CTA has read the amax word
-    if (threadIdx.x == 0) {
-      __threadfence();
-      if (atomicAdd(ws + 1, 1u) == gridDim.x - 1u) {  // last CTA: all CTAs have read it
-        ws[0] = 0u;
-        ws[1] = 0u;
-      }
-    }
-  }
+  __shared__ float inv_tab[128];     // fp32(1 / fp32(dec(s) ts)) per E4M3 code s (0: zero block)
+  __shared__ uint32_t code_tab[128];  // code stored for s (0 for a zero block)
+  const float ts = ts_in != nullptr
+                       ? *ts_in
+                       : __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile unsigned*>(ws)), kTsDivisor);
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
-  const float six_ts = __fmul_rn(6.0f, ts);
+  build_scale_tables(ts, inv_tab, code_tab);
+  const ScaleRoute sr = scale_route(ts);
+  __syncthreads();
+
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = (blockIdx.x * kQuantThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kQuantThreads) >> 5;
   const uint32_t gpr = blocks_per_row >> 2;
   const uint64_t row_code_bytes = (uint64_t)blocks_per_row * 8u;
+  const uint32_t lane_sf = (lane >> 2) * 512u + (lane & 3u);  // this lane's byte in 8 scale atoms
+  const int32_t cpr = static_cast<int32_t>(chunks_per_row);
+  // slot u visits items total - 1 - (warp + u * nwarps + k * step), k = 0, 1, ...; its
+  // (row, chunk) is stepped without a division
+  const int32_t step = static_cast<int32_t>(nwarps * kQuantUnroll);
+  const int32_t step_rows = step / cpr, step_chunks = step % cpr;
+  int32_t row[kQuantUnroll], chunk[kQuantUnroll];
+#pragma unroll
+  for (int u = 0; u < kQuantUnroll; ++u) {
+    const int32_t item = static_cast<int32_t>(total_items) - 1 - static_cast<int32_t>(warp + u * nwarps);
+    row[u] = item >= 0 ? item / cpr : -1;
+    chunk[u] = item >= 0 ? item % cpr : 0;
+  }
 
-  for (uint32_t base = warp; base < total_items; base += nwarps * kQuantUnroll) {
+  while (row[0] >= 0) {  // slot 0 holds the largest remaining item
     uint4 lo[kQuantUnroll], hi[kQuantUnroll];
-    QuantItem q[kQuantUnroll];
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      const uint32_t i = base + u * nwarps;
-      const bool in = i < total_items;
-      q[u] = quant_item(in ? total_items - 1u - i : 0u, lane, M, blocks_per_row, chunks_per_row);
-      q[u].live = q[u].live && in;
-      q[u].real = q[u].real && in;
+      const uint32_t blk = static_cast<uint32_t>(chunk[u]) * 32u + lane;
       lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (q[u].real) {
-        const __nv_bfloat16* src = x + q[u].row * ldx + q[u].blk * 16u;
+      if (row[u] >= 0 && static_cast<uint32_t>(row[u]) < M && blk < blocks_per_row) {
+        const __nv_bfloat16* src = x + static_cast<uint64_t>(row[u]) * ldx + blk * 16u;
         if (kLoad32) {
           ld_nc_v8(src, lo[u], hi[u]);
         } else {
@@ -209,18 +268,182 @@ __global__ void __launch_bounds__(kQuantThreads)
     }
 #pragma unroll
     for (int u = 0; u < kQuantUnroll; ++u) {
-      if (!q[u].live) continue;
-      uint32_t scale = 0u;
-      if (q[u].real) {
-        const BlockScale bs = block_scale(fmaxf(absmax8(lo[u]), absmax8(hi[u])), ts, six_ts);
-        uint2 c = make_uint2(0u, 0u);
-        if (bs.live) c = make_uint2(encode8(lo[u], bs.inv), encode8(hi[u], bs.inv));
-        *reinterpret_cast<uint2*>(codes + q[u].row * row_code_bytes + q[u].blk * 8u) = c;
-        scale = bs.code;
+      const int32_t r = row[u];
+      const uint32_t blk = static_cast<uint32_t>(chunk[u]) * 32u + lane;
+      if (r >= 0 && blk < blocks_per_row) {
+        const uint32_t ru = static_cast<uint32_t>(r);
+        uint32_t stored = 0u;
+        if (ru < M) {
+          uint2 c;
+          stored = quantize_block(lo[u], hi[u], sr, inv_tab, code_tab, c);
+          *reinterpret_cast<uint2*>(codes + ru * row_code_bytes + blk * 8u) = c;
+        }
+        scales[((ru >> 7) * gpr + static_cast<uint32_t>(chunk[u]) * 8u) * 512u + (ru & 31u) * 16u +
+               ((ru >> 5) & 3u) * 4u + lane_sf] = static_cast<uint8_t>(stored);
       }
-      const uint32_t r = q[u].row, b = q[u].blk;
-      scales[((r >> 7) * gpr + (b >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (b & 3u)] =
-          static_cast<uint8_t>(scale);
+      chunk[u] -= step_chunks;
+      row[u] -= step_rows;
+      if (chunk[u] < 0) {
+        chunk[u] += cpr;
+        row[u] -= 1;
+      }
+    }
+  }
+  if (ts_in == nullptr) {
+    __syncthreads();  // every thread of this CTA has read the amax word (long ago)
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(ws + 1, 1u) == gridDim.x - 1u) {  // last CTA: all CTAs have read it
+        ws[0] = 0u;
+        ws[1] = 0u;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Single-pass quantizer for activations that fit in the shared memory of the whole GPU (a
+// dynamic tensor scale only): one cooperative launch, one CTA per SM. CTA b bulk-copies
+// rows [b R, b R + R) of x into its shared memory (one copy and one mbarrier per row),
+// reduces their amax while the rows land, and joins a grid-wide barrier on workspace words
+// (bounded spin; the cooperative launch guarantees every CTA is resident). It then reads the
+// tensor amax and quantizes its rows from shared memory: x is read from HBM once, in one
+// launch, instead of twice in two.
+//
+// Workspace words: ws[0] amax bits (atomic max), ws[1] CTAs arrived, ws[2] CTAs departed,
+// ws[3] failure flag. The CTA that departs last has seen every CTA pass the barrier and zeroes
+// all four. A wait that runs out of time marks the failure: every CTA then writes no codes and
+// the tensor scale written is NaN.
+// ---------------------------------------------------------------------------------------
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedWarps = kFusedThreads / 32;
+constexpr int kFusedMaxRows = 64;               // rows per CTA (one mbarrier each)
+constexpr int kFusedSmemData = 200 * 1024;      // bytes of x per CTA
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    quantize_fused_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M, uint32_t Mpad,
+                          uint32_t K, uint32_t rows_per_cta, uint8_t* __restrict__ codes,
+                          uint8_t* __restrict__ scales, unsigned* ws, float* __restrict__ ts_out,
+                          uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t xs[];  // rows_per_cta rows of x, K * 2 bytes each
+  __shared__ __align__(8) uint64_t row_bar[kFusedMaxRows];
+  __shared__ float inv_tab[128];
+  __shared__ uint32_t code_tab[128];
+  __shared__ uint32_t warp_max[kFusedWarps];
+  __shared__ float ts_s;
+  __shared__ int failed;
+
+  const uint32_t r0 = blockIdx.x * rows_per_cta;
+  const uint32_t r_end = min(Mpad, r0 + rows_per_cta);  // rows [r0, r_end), padding included
+  const uint32_t n_real = min(M, r_end) > r0 ? min(M, r_end) - r0 : 0u;  // rows holding data
+  const uint32_t row_bytes = K * 2u;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+
+  if (threadIdx.x == 0) failed = 0;
+  if (threadIdx.x < n_real) mbar_init(smem_u32(&row_bar[threadIdx.x]), 1);
+  fence_mbarrier_init();
+  __syncthreads();
+  // warp w copies and then reduces rows w, w + 32, ...
+  if (lane == 0) {
+    const uint64_t pol = policy_evict_first();
+    for (uint32_t i = warp; i < n_real; i += kFusedWarps) {
+      const uint32_t bar = smem_u32(&row_bar[i]);
+      mbar_arrive_expect_tx(bar, row_bytes);
+      bulk_load_hint(smem_u32(xs + i * row_bytes), x + (uint64_t)(r0 + i) * ldx, row_bytes, bar, pol);
+    }
+  }
+
+  uint32_t m = 0u;
+  bool ok = true;
+  for (uint32_t i = warp; i < n_real && ok; i += kFusedWarps) {
+    ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&row_bar[i]), 0u, timeout_ns, nullptr));
+    if (!ok) break;
+    const uint4* row = reinterpret_cast<const uint4*>(xs + i * row_bytes);
+    for (uint32_t v = lane; v < K / 8u; v += 32u) {
+      const uint4 q = row[v];
+      m = bf16x2_max_abs(m, bf16x2_max_abs(bf16x2_max_abs(q.x, q.y), bf16x2_max_abs(q.z, q.w)));
+    }
+  }
+  if (!ok && lane == 0) failed = 1;
+  uint32_t h = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
+  h = __reduce_max_sync(0xFFFFFFFFu, h);
+  if (lane == 0) warp_max[warp] = h;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t cm = 0u;
+    for (int w = 0; w < kFusedWarps; ++w) cm = max(cm, warp_max[w]);
+    // publish the amax (and a failure), then arrive; the release orders them before it
+    if (cm != 0u) red_max_relaxed_gpu(ws, cm << 16);
+    if (failed) red_or_relaxed_gpu(ws + 3, 1u);
+    red_add_release_gpu(ws + 1, 1u);
+    // grid barrier: every CTA has published its amax
+    const uint64_t t0 = global_timer_ns();
+    bool all_in = false;
+    while (!(all_in = ld_acquire_gpu(ws + 1) >= gridDim.x)) {
+      if (global_timer_ns() - t0 > timeout_ns) break;
+    }
+    __threadfence();
+    const bool bad = !all_in || ld_acquire_gpu(ws + 3) != 0u;
+    const uint32_t amax_bits = ld_acquire_gpu(ws);
+    failed = bad ? 1 : 0;
+    ts_s = bad ? __int_as_float(0x7FC00000) : __fdiv_rn(__uint_as_float(amax_bits), kTsDivisor);
+  }
+  __syncthreads();
+  const float ts = ts_s;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
+  if (!failed) {
+    build_scale_tables(ts, inv_tab, code_tab);
+    const ScaleRoute sr = scale_route(ts);
+    __syncthreads();
+    // quantize: item = (row, 512-element chunk); lane = one 16-element block of the chunk;
+    // a warp takes two items at a time
+    const uint32_t bpr = K / 16u, cpr = (bpr + 31u) / 32u, gpr = bpr >> 2;
+    const uint32_t items = (r_end - r0) * cpr;
+    const uint64_t row_code_bytes = (uint64_t)bpr * 8u;
+    for (uint32_t it0 = warp; it0 < items; it0 += 2 * kFusedWarps) {
+      uint4 lo[2], hi[2];
+      uint32_t rr[2], bb[2];
+      bool data[2], valid[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t it = it0 + u * kFusedWarps;
+        const uint32_t i = it / cpr;
+        bb[u] = (it - i * cpr) * 32u + lane;
+        rr[u] = r0 + i;
+        valid[u] = it < items && bb[u] < bpr;
+        data[u] = valid[u] && i < n_real;
+        lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (data[u]) {
+          const uint4* src = reinterpret_cast<const uint4*>(xs + i * row_bytes + bb[u] * 32u);
+          lo[u] = src[0];
+          hi[u] = src[1];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (!valid[u]) continue;
+        uint32_t stored = 0u;
+        if (data[u]) {
+          uint2 c;
+          stored = quantize_block(lo[u], hi[u], sr, inv_tab, code_tab, c);
+          *reinterpret_cast<uint2*>(codes + rr[u] * row_code_bytes + bb[u] * 8u) = c;
+        }
+        scales[scale_offset(rr[u], bb[u], gpr)] = static_cast<uint8_t>(stored);
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // copies still in flight (after a failed wait) must land before the CTA exits
+    if (failed)
+      for (uint32_t i = 0; i < n_real; ++i) (void)mbar_wait(smem_u32(&row_bar[i]), 0u, timeout_ns, nullptr);
+    // every CTA that departs has passed the grid barrier and read the words; the last one
+    // to depart resets them for the next call
+    if (atomicAdd(ws + 2, 1u) == gridDim.x - 1u) {
+      ws[0] = 0u;
+      ws[1] = 0u;
+      ws[2] = 0u;
+      ws[3] = 0u;
     }
   }
 }
@@ -316,9 +539,50 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
   return cudaGetLastError();
 }
 
+namespace {
+
+// Rows per CTA of the single-pass quantizer for x [M, K] (0: x does not fit, or the copies
+// cannot be bulk copies).
+uint32_t fused_rows_per_cta(const void* x, int64_t M, int64_t K, int64_t ldx) {
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || (ldx * 2) % 16 != 0) return 0;
+  static const int per_sm = [] {
+    int n = 0;
+    if (cudaFuncSetAttribute(quantize_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kFusedSmemData) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quantize_fused_kernel, kFusedThreads, kFusedSmemData) !=
+            cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+    return n;
+  }();
+  if (per_sm < 1) return 0;
+  const int64_t mpad = (M + 127) / 128 * 128;
+  const int64_t ctas = static_cast<int64_t>(sm_count()) * per_sm;
+  const int64_t rows = (mpad + ctas - 1) / ctas;
+  if (rows > kFusedMaxRows || rows * K * 2 > kFusedSmemData) return 0;
+  return static_cast<uint32_t>(rows);
+}
+
+}  // namespace
+
 cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                             uint8_t* scales, unsigned* ws, const float* ts_in, float* ts_out,
                             cudaStream_t s) {
+  if (ts_in == nullptr && M > 0) {
+    if (const uint32_t rows = fused_rows_per_cta(x, M, K, ldx); rows != 0) {
+      const int64_t mpad = (M + 127) / 128 * 128;
+      const unsigned grid = static_cast<unsigned>((mpad + rows - 1) / rows);
+      const __nv_bfloat16* xp = static_cast<const __nv_bfloat16*>(x);
+      uint64_t ld = static_cast<uint64_t>(ldx);
+      uint32_t m = static_cast<uint32_t>(M), mp = static_cast<uint32_t>(mpad), k = static_cast<uint32_t>(K);
+      uint32_t r = rows;
+      uint64_t limit = wait_timeout_ns();
+      void* args[] = {&xp, &ld, &m, &mp, &k, &r, &codes, &scales, &ws, &ts_out, &limit};
+      return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(quantize_fused_kernel), dim3(grid),
+                                         dim3(kFusedThreads), args, static_cast<size_t>(rows) * K * 2, s);
+    }
+  }
   if (ts_in == nullptr) {
     const cudaError_t e = launch_amax(x, M, K, ldx, ws, s);
     if (e != cudaSuccess) return e;
