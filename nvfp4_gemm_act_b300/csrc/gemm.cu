@@ -13,23 +13,31 @@
 // tile, so a 256-deep pipeline stage is 38 KB per SM (5 stages in flight). Pairs walk
 // (row-tile pair, weight tile) tiles round-robin, row pairs fastest, so concurrent pairs
 // share weight tiles in L2.
-//   warp 0     (both CTAs) TMA producer: this CTA's A tile, its half of the B tile, its A
-//              scale tile, and one of the two B scale bands multicast to both CTAs (every
-//              CTA needs the scales of all 256 columns in its TMEM); all of them complete on
-//              the leader CTA's full barrier; L2 prefetch 8 k-blocks ahead;
+//   warp 0     (both CTAs) TMA producer of the codes: this CTA's A tile and its half of
+//              the B tile;
+//   warp 6     (both CTAs) TMA producer of the scales: this CTA's A scale tile and one of
+//              the two B scale bands, multicast to both CTAs (every CTA needs the scales of
+//              all 256 columns in its TMEM). Both producers' loads complete on the leader
+//              CTA's full barrier, where each of the leader's two producers announces its
+//              bytes for both CTAs;
 //   warp 1     (both CTAs) TMEM allocation (pair-collective); in the leader, the single
 //              MMA-issuing thread, whose commits release the stage and publish the
 //              accumulator in both CTAs;
-//   warps 2-3  (leader) block-scale copies shared -> TMEM (tcgen05.cp.cta_group::2 copies
-//              each CTA's own shared block into its own TMEM), split between two warps and
-//              running a stage ahead of the MMA warp: a copy costs its issuing thread about
-//              as long as an MMA, so the MMA thread must not issue them;
-//   warps 4-11 (both CTAs) epilogue: TMEM lane = output row; two warps per 32-lane quarter,
+//   warps 2-5  (leader) block-scale copies shared -> TMEM (tcgen05.cp.cta_group::2 copies
+//              each CTA's own shared block into its own TMEM), warp 2 + j taking 64-deep
+//              k-step j of every stage and running ahead of the MMA warp. A copy occupies its
+//              issuing thread for about 120 cycles while copies from other warps do not slow
+//              the MMAs, so the 12 copies of a 256-deep stage are spread over four warps;
+//   warp 7     no role;
+//   warps 8-15 (both CTAs) epilogue: TMEM lane = output row; two warps per 32-lane quarter,
 //              one per 128-column half. Each thread pulls its 128 accumulator columns into
 //              registers, then reports TMEM free to the leader, so the next tile's MMAs run
 //              while it applies the epilogue and stores. Per-head RMSNorm sums are
 //              thread-local, combined across the two halves through shared memory when a
 //              head spans the whole tile.
+// Registers: warpgroups 0-1 drop to 72 per thread (setmaxnreg) so that warpgroups 2-3 can
+// hold a 128-column accumulator slice (176 per thread); 4 x 32 x (2 x 72 + 2 x 176) = 63488
+// of the 512 x 128 the block is launched with.
 // Every wait is bounded (NVFP4_ERR_TIMEOUT in *err on expiry; the CTA then drains what it
 // issued, frees TMEM and exits).
 
@@ -53,7 +61,6 @@ constexpr int kBKBytes = kBK / 2;        // 128: one 128-byte swizzle row of pac
 constexpr int kStages = 5;
 constexpr int kMmaK = 64;                // K per tcgen05.mma (kind::mxf4nvf4)
 constexpr int kKStepsPerStage = kBK / kMmaK;
-constexpr int kPrefetchDist = 8;         // k-blocks prefetched into L2 ahead of the ring
 constexpr int kCluster = 2;              // the CTA pair of the 2-SM MMA
 constexpr int kBRowsPerCta = kBN / kCluster;
 
@@ -62,15 +69,21 @@ constexpr int kBBytes = kBRowsPerCta * kBKBytes;              // 16 KB (this CTA
 constexpr int kSfAtom = 512;                                  // 128 rows x 4 scales
 constexpr int kSfaBytes = kKStepsPerStage * kSfAtom;          // 2 KB
 constexpr int kSfbBytes = (kBN / 128) * kKStepsPerStage * kSfAtom;  // 4 KB: both bands
-constexpr int kStageTx = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // bytes per CTA per stage
 
-constexpr int kSfWarps = 2;              // warps issuing the scale copies (shared -> TMEM)
-constexpr int kEpiWarp0 = 2 + kSfWarps;  // first epilogue warp
+constexpr int kSfWarps = 4;              // warps issuing the scale copies (shared -> TMEM)
+constexpr int kSfWarp0 = 2;
+constexpr int kEpiWarp0 = 8;             // first epilogue warp (warpgroups 2 and 3)
 constexpr int kEpiWarps = 8;
+// register split (setmaxnreg on entering each role): warpgroups 0-1 lean, 2-3 epilogue
+constexpr uint32_t kRegsLean = 72;
+constexpr uint32_t kRegsEpilogue = 176;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kThreads = kEpiWarp0 * 32 + kEpiThreads;
 constexpr int kHalf = kBN / 2;           // columns per epilogue warp
 static_assert(kEpiWarp0 % 4 == 0, "epilogue warps must start on a warpgroup (TMEM lane quarters)");
+static_assert(kThreads == 512 && kEpiWarp0 == 8, "two lean and two epilogue warpgroups");
+// the split must fit in what the block is launched with (512 threads x 128 registers)
+static_assert(128u * (2 * kRegsLean + 2 * kRegsEpilogue) <= 512u * 128u, "register split");
 
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kStages * kABytes;
@@ -277,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_sfa);
     prefetch_tmap(&tm_sfb);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);            // the leader's producer arrival (+ both CTAs' bytes)
+      mbar_init(full_bar(s), 2);            // the leader's two producers' arrivals (+ both CTAs' bytes)
       mbar_init(empty_bar(s), 1);           // the leader's MMA commit
       mbar_init(sf_bar(s), kSfWarps);       // one commit from each scale-copy warp
     }
@@ -297,49 +310,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer (both CTAs) ----------------
-      const uint64_t pol = policy_evict_normal();
-      uint32_t kc = 0;  // k-blocks issued so far (ring position)
-      bool ok = true;
-      for (int pt = cluster_id; pt < num_tiles && ok; pt += num_clusters) {
-        const int m_blk = (pt % num_pairs_m) * kCluster + rank;  // rows past M load as zeros
-        const int n_blk = pt / num_pairs_m;
-        const int b_row = n_blk * kBN + rank * kBRowsPerCta;
-        for (int kb = 0; kb < min(num_k_blocks, kPrefetchDist); ++kb) {
-          tma_prefetch_2d(&tm_a, kb * kBKBytes, m_blk * kBM);
-          tma_prefetch_2d(&tm_b, kb * kBKBytes, b_row);
+  // ---------------- TMA producers (both CTAs) ----------------
+  // warp 0: this CTA's A tile and its half of the B tile; warp 6:
+  // its A scale tile and one of the two B scale bands, multicast to both CTAs (every CTA
+  // needs the scales of all 256 columns). Both complete on the leader CTA's full barrier,
+  // on which each producer of the leader announces its bytes for both CTAs.
+  auto producer = [&](const bool codes_part) {
+    const uint64_t pol = policy_evict_normal();
+    uint32_t kc = 0;  // k-blocks issued so far (ring position)
+    bool ok = true;
+    for (int pt = cluster_id; pt < num_tiles && ok; pt += num_clusters) {
+      const int m_blk = (pt % num_pairs_m) * kCluster + rank;  // rows past M load as zeros
+      const int n_blk = pt / num_pairs_m;
+      const int b_row = n_blk * kBN + rank * kBRowsPerCta;
+      for (int kb = 0; kb < num_k_blocks; ++kb) {
+        const int s = kc % kStages;
+        if (!mbar_wait(empty_bar(s), ((kc / kStages) & 1u) ^ 1u, timeout_ns, err)) {
+          ok = false;
+          break;
         }
-        for (int kb = 0; kb < num_k_blocks; ++kb) {
-          if (kb + kPrefetchDist < num_k_blocks) {
-            tma_prefetch_2d(&tm_a, (kb + kPrefetchDist) * kBKBytes, m_blk * kBM);
-            tma_prefetch_2d(&tm_b, (kb + kPrefetchDist) * kBKBytes, b_row);
-          }
-          const int s = kc % kStages;
-          if (!mbar_wait(empty_bar(s), ((kc / kStages) & 1u) ^ 1u, timeout_ns, err)) {
-            ok = false;
-            break;
-          }
-          const uint32_t bar = mapa_shared(full_bar(s), 0);  // the leader's full barrier
-          if (leader) mbar_arrive_expect_tx(full_bar(s), kCluster * kStageTx);
+        const uint32_t bar = mapa_shared(full_bar(s), 0);  // the leader's full barrier
+        if (codes_part) {
+          if (leader) mbar_arrive_expect_tx(full_bar(s), kCluster * (kABytes + kBBytes));
           tma_load_2d_pair(sbase + kOffA + s * kABytes, &tm_a, kb * kBKBytes, m_blk * kBM, bar, pol);
           tma_load_2d_pair(sbase + kOffB + s * kBBytes, &tm_b, kb * kBKBytes, b_row, bar, pol);
+        } else {
+          if (leader) mbar_arrive_expect_tx(full_bar(s), kCluster * (kSfaBytes + kSfbBytes));
           // scale tiles: row = band * k_atoms + first k-atom of the stage (4 atoms of 512 B)
           tma_load_2d_pair(sbase + kOffSfa + s * kSfaBytes, &tm_sfa, 0,
                            m_blk * k_atoms + kb * kKStepsPerStage, bar, pol);
-          // B scale band `rank` of the tile, multicast to both CTAs (each needs both bands)
           tma_load_2d_pair_mc(sbase + kOffSfb + s * kSfbBytes + rank * (kSfbBytes / 2), &tm_sfb, 0,
                               (n_blk * 2 + rank) * k_atoms + kb * kKStepsPerStage, bar, 0x3, pol);
-          ++kc;
         }
+        ++kc;
       }
-      // Before exit: the leader's MMA has released every stage this CTA filled, so all its
-      // copies have landed and all the leader's arrivals on this CTA's barriers are made.
-      for (uint32_t i = kc > (uint32_t)kStages ? kc - kStages : 0u; i < kc; ++i)
-        (void)mbar_wait(empty_bar(i % kStages), (i / kStages) & 1u, timeout_ns, err);
     }
+    // Before exit: the leader's MMA has released every stage this CTA filled, so all its
+    // copies have landed and all the leader's arrivals on this CTA's barriers are made.
+    for (uint32_t i = kc > (uint32_t)kStages ? kc - kStages : 0u; i < kc; ++i)
+      (void)mbar_wait(empty_bar(i % kStages), (i / kStages) & 1u, timeout_ns, err);
+  };
+
+  if (warp == 0) {
+    warpgroup_reg_dealloc<kRegsLean>();
+    if (lane == 0) producer(true);
   } else if (warp == 1) {
+    warpgroup_reg_dealloc<kRegsLean>();
     if (lane == 0 && leader) {
       // ---------------- MMA issuer (leader) ----------------
       uint32_t kc = 0;
@@ -377,13 +393,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit_pair(drain_bar);
       (void)mbar_wait(drain_bar, 0u, timeout_ns, err);
     }
-  } else if (warp < kEpiWarp0) {
+  } else if (warp < kSfWarp0 + kSfWarps) {
+    warpgroup_reg_dealloc<kRegsLean>();
     if (lane == 0 && leader) {
       // ---------------- block-scale copies, shared -> TMEM (leader, for both CTAs) --------
-      // scale warp w copies, per 64-deep k-step, B scale band w and the A scales of
-      // k-steps {2w, 2w+1}; the TMEM slot of stage s is free again once stage s has been
-      // refilled (the refill waited for the MMAs that read the previous scales).
-      const int w = warp - 2;
+      // scale warp w copies the scales of 64-deep k-step w of each stage: A, B band 0, B
+      // band 1; the TMEM slot of stage s is free again once stage s has been refilled (the
+      // refill waited for the MMAs that read the previous scales).
+      const int w = warp - kSfWarp0;
       uint32_t kc = 0;
       bool ok = true;
       for (int pt = cluster_id; pt < num_tiles && ok; pt += num_clusters) {
@@ -398,11 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sf_col = tmem_base + kSfCol0 + s * kSfColsPerStage;
           const uint32_t sfa_s = sbase + kOffSfa + s * kSfaBytes;
           const uint32_t sfb_s = sbase + kOffSfb + s * kSfbBytes;
-          for (int j = 0; j < nk; ++j) {
-            if ((j >> 1) == w)
-              tmem_cp_32x128b_x4_pair(sf_col + j * 4, smem_desc(sfa_s + j * kSfAtom, 128, 128, kSwizzleNone));
-            tmem_cp_32x128b_x4_pair(sf_col + kSfaColsPerStage + j * 8 + w * 4,
-                                    smem_desc(sfb_s + w * (kSfbBytes / 2) + j * kSfAtom, 128, 128, kSwizzleNone));
+          for (int j = w; j < nk; j += kSfWarps) {
+            tmem_cp_32x128b_x4_pair(sf_col + j * 4, smem_desc(sfa_s + j * kSfAtom, 128, 128, kSwizzleNone));
+#pragma unroll
+            for (int h = 0; h < kBN / 128; ++h)
+              tmem_cp_32x128b_x4_pair(sf_col + kSfaColsPerStage + j * 8 + h * 4,
+                                      smem_desc(sfb_s + h * (kSfbBytes / 2) + j * kSfAtom, 128, 128, kSwizzleNone));
           }
           tc_commit_pair(sf_bar(s));
           ++kc;
@@ -411,8 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit_pair(sf_drain_bar);
       (void)mbar_wait(sf_drain_bar, 0u, timeout_ns, err);
     }
+  } else if (warp < kEpiWarp0) {
+    // warp 6: scale-tile producer; warp 7: no role (it fills warpgroup 1)
+    warpgroup_reg_dealloc<kRegsLean>();
+    if (warp == kEpiWarp0 - 2 && lane == 0) producer(false);
   } else {
     // ---------------- epilogue warps (both CTAs) ----------------
+    warpgroup_reg_alloc<kRegsEpilogue>();
     const int ew = warp - kEpiWarp0;       // 0..7
     const int q = warp & 3;                // TMEM lane quarter this warp may access
     const int half = ew >> 2;              // which 128-column half of the tile
@@ -545,6 +568,11 @@ nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // the setmaxnreg split assumes the block is launched with 128 registers per thread: with
+    // fewer, the epilogue warpgroups' increase could never be granted
+    cudaFuncAttributes fa;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, gemm_nvfp4_kernel);
+    if (attr_err == cudaSuccess && fa.numRegs != 128) attr_err = cudaErrorInvalidConfiguration;
   });
   if (attr_err != cudaSuccess) return NVFP4_ERR_LAUNCH;
   EpiParams ep;

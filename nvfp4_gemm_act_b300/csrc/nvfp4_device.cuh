@@ -202,6 +202,17 @@ __device__ __forceinline__ void red_add_release_gpu(unsigned* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Per-thread register budget of the calling warp's warpgroup (every warp of the warpgroup
+// executes the same call): give registers back to the block's pool / take them from it.
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kRegs) : "memory");
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_reg_alloc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kRegs) : "memory");
+}
+
 // Acquire load of a global word at GPU scope.
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned* p) {
   uint32_t v;

@@ -170,3 +170,45 @@ def test_rows_only_16_byte_aligned():
     assert view.data_ptr() % 32 == 16
     q = nv.nvfp4_quantize(view)
     assert_quant_equal(gpu_nvfp4_to_np(q), R.quantize_ref(to_np_f32(x)), "16-byte aligned rows")
+
+
+def _boundary_blocks(k: int, rng, with_neighbours=True):
+    """Rows of 16-element blocks whose |max| is an E4M3 value or a midpoint between two, times
+    2^k (exact in bf16), and its bf16 neighbours: with 6 ts = 2^k the block quotient lands on
+    the E4M3 rounding boundaries, where the kernels' reciprocal route must defer to the exact
+    division."""
+    vals = R.e4m3_decode(np.arange(127, dtype=np.uint8)).astype(np.float64)
+    targets = np.concatenate([vals, (vals[:-1] + vals[1:]) / 2]) * 2.0 ** k
+    t16 = torch.from_numpy(targets.astype(np.float32)).to(torch.bfloat16)
+    assert np.array_equal(t16.float().numpy().astype(np.float64), targets), "targets exact in bf16"
+    bits = t16.view(torch.int16).numpy().astype(np.int32)
+    if with_neighbours:
+        bits = np.concatenate([bits, bits + 1, np.maximum(bits - 1, 0)])
+    mags = torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).float().numpy()
+    n = mags.size
+    x = rng.uniform(-1.0, 1.0, (n, 16)) * mags[:, None] * 0.9
+    x[np.arange(n), rng.integers(0, 16, n)] = mags * rng.choice([-1.0, 1.0], n)
+    rows = -(-n * 16 // 256)
+    flat = np.zeros(rows * 256)
+    flat[: n * 16] = x.ravel()
+    return flat.reshape(rows, 256)
+
+
+@pytest.mark.parametrize("k", [0, -3, 5, -9])
+def test_scale_rounding_boundaries_static_scale(k):
+    # two-launch path; 6 * fp32(2^k / 6) rounds to exactly 2^k
+    ts = np.float32(2.0 ** k / 6.0)
+    assert np.float32(6.0) * ts == np.float32(2.0 ** k)
+    x = _bf16(_boundary_blocks(k, np.random.default_rng(40 + k)))
+    quant_both(x, ts_in=ts, what=f"E4M3 boundaries, static ts, k={k}")
+
+
+@pytest.mark.parametrize("k", [0, -4, 6])
+def test_scale_rounding_boundaries_dynamic_scale(k):
+    # single-launch path: one element of 448 * 2^k pins amax, so ts = fp32(2^k / 6)
+    xb = _boundary_blocks(k, np.random.default_rng(60 + k))
+    xb = np.clip(xb, -448.0 * 2.0 ** k, 448.0 * 2.0 ** k)
+    xb[0, 0] = 448.0 * 2.0 ** k
+    x = _bf16(xb)
+    q = quant_both(x, what=f"E4M3 boundaries, dynamic ts, k={k}")
+    assert np.float32(6.0) * gpu_nvfp4_to_np(q)[2] == np.float32(2.0 ** k)
