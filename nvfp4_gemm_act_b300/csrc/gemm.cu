@@ -367,9 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int kb = 0; kb < num_k_blocks; ++kb) {
           const int s = kc % kStages;
-          // operands of both CTAs landed, and their scales are in both TMEMs
-          if (!mbar_wait(full_bar(s), (kc / kStages) & 1u, timeout_ns, err) ||
-              !mbar_wait(sf_bar(s), (kc / kStages) & 1u, timeout_ns, err)) {
+          // the scales are in both TMEMs: the scale warps commit sf_bar only after they saw
+          // the stage's full barrier, so the operands of both CTAs have landed too
+          if (!mbar_wait(sf_bar(s), (kc / kStages) & 1u, timeout_ns, err)) {
             ok = false;
             break;
           }
