@@ -345,9 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++kc;
       }
     }
-    // Before exit: the leader's MMA has released every stage this CTA filled, so all its
-    // copies have landed and all the leader's arrivals on this CTA's barriers are made.
-    for (uint32_t i = kc > (uint32_t)kStages ? kc - kStages : 0u; i < kc; ++i)
+    // Before exit, no copy may still be in flight into either CTA's shared memory, and no
+    // arrival of the leader may still be on its way to this CTA's barriers. The copies of both
+    // CTAs complete on the leader's full barriers: the leader waits for the stages it issued
+    // last (the follower stays until the leader reaches the closing cluster barrier); every
+    // CTA waits for the leader's release of its stages (the MMA commits arrive on them).
+    // On the normal path all of these have completed already; after a timed-out wait they
+    // are waited for again, each within the time limit.
+    const uint32_t first = kc > (uint32_t)kStages ? kc - kStages : 0u;
+    if (leader)
+      for (uint32_t i = first; i < kc; ++i)
+        (void)mbar_wait(full_bar(i % kStages), (i / kStages) & 1u, timeout_ns, err);
+    for (uint32_t i = first; i < kc; ++i)
       (void)mbar_wait(empty_bar(i % kStages), (i / kStages) & 1u, timeout_ns, err);
   };
 
