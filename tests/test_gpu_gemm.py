@@ -99,3 +99,17 @@ def test_gated_output_pairs_match_unpermuted_formula():
     torch.cuda.synchronize()
     ref = R.gated_silu_ref(to_np_f32(plain).astype(np.float64))
     assert_fp32_close(g, ref, "gated vs formula on plain GEMM")
+
+
+MANY_TILE_ROWS = np.unique(np.concatenate([[0, 127, 128, 255, 256, 2047, 2048, 4095],
+                                           np.random.default_rng(13).integers(0, 4096, 24)]))
+
+
+@pytest.mark.parametrize("epi", ["bias", "head_rmsnorm", "gated_silu"])
+def test_many_tiles_per_pair_partial_stage(epi):
+    # 16 x 9 = 144 pair tiles on 74 CTA pairs (two tiles for most pairs) with K = 1344: six
+    # 256-deep stages per tile, the last holding one 64-deep step, so the 5-slot ring's
+    # position drifts against tile boundaries and the accumulator handshake alternates phase
+    norm_cols = 1536 if epi == "head_rmsnorm" else 0
+    w = W.Workload(f"many_{epi}", 4096, 1344, 2304, epi, seed=77, norm_cols=norm_cols, head_dim=64)
+    check_case(w, rows=MANY_TILE_ROWS)
