@@ -183,6 +183,31 @@ NVFP4_API nvfp4_status nvfp4_gemm(const uint8_t *a_codes, const uint8_t *a_scale
                         int64_t norm_cols, float eps, nvfp4_out_dtype out_dtype, void *out,
                         int64_t ldo, int *device_error, nvfp4_stream_t stream);
 
+/*
+ * nvfp4_gemm_nvfp4_out -- the same GEMM and epilogue, writing the output as NVFP4 for the
+ * next layer instead of bf16/fp32: no bf16 round trip through HBM between two FP4 layers
+ * (page "How fal made Ideogram V4 6x faster", NVFP4 paragraph: a 4-bit matmul only pays off
+ * when the bytes around it shrink too, so the quantize of a layer's output belongs in the
+ * producing kernel).
+ *
+ *   out_tensor_scale  fp32 [1] device: the output's STATIC tensor scale ts_out (a dynamic
+ *          scale would need the whole output's amax before the first block is coded; a
+ *          caller can use, e.g., a calibrated value or the previous step's amax / 2688).
+ *   out_codes   uint8 [M, W/2] contiguous, W = output width (N, or N/2 for GATED_SILU).
+ *   out_scales  nvfp4_scales_bytes(M, W) bytes, tiled layout; padding rows written 0.
+ * Each output value is first rounded to bf16 exactly as the bf16 output mode stores it, then
+ * the 16-blocks along a row are quantized as nvfp4_quantize does with tensor_scale_in =
+ * out_tensor_scale: the codes and scales are identical to nvfp4_gemm(..., NVFP4_OUT_BF16)
+ * followed by nvfp4_quantize(y, static ts), and feed nvfp4_gemm as its A operand (K = W).
+ * Rules: those of nvfp4_gemm, plus W % 64 == 0; out_codes and out_scales 16-byte aligned.
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_nvfp4_out(const uint8_t *a_codes, const uint8_t *a_scales,
+                        const float *a_ts, const uint8_t *b_codes, const uint8_t *b_scales,
+                        const float *b_ts, int64_t M, int64_t N, int64_t K, nvfp4_epilogue epi,
+                        const float *bias, const float *gamma, int head_dim, int64_t norm_cols,
+                        float eps, const float *out_tensor_scale, uint8_t *out_codes,
+                        uint8_t *out_scales, int *device_error, nvfp4_stream_t stream);
+
 /* Synchronizes `stream`, copies *device_error to *code, then zeroes the device word.
  * Returns NVFP4_ERR_NULL for NULL pointers, NVFP4_ERR_LAUNCH if a CUDA call fails. */
 NVFP4_API nvfp4_status nvfp4_get_device_error(int *device_error, int *code, nvfp4_stream_t stream);

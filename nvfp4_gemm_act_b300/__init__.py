@@ -37,6 +37,8 @@ _SIGS = {
     "nvfp4_pack_weights": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_int, _P, _P, _P, _P, _P]),
     "nvfp4_gemm": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P,
                                   ctypes.c_int, _I64, ctypes.c_float, ctypes.c_int, _P, _I64, _P, _P]),
+    "nvfp4_gemm_nvfp4_out": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P,
+                                            ctypes.c_int, _I64, ctypes.c_float, _P, _P, _P, _P, _P]),
     "nvfp4_get_device_error": (ctypes.c_int, [_P, _P, _P]),
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
@@ -156,6 +158,28 @@ def nvfp4_gemm(a: Nvfp4Tensor, b: Nvfp4Tensor, epilogue: str = "bias",
         _ptr(a.codes), _ptr(a.scales), _ptr(a.ts), _ptr(b.codes), _ptr(b.scales), _ptr(b.ts),
         M, N, K, EPILOGUES[epilogue], _ptr(bias), _ptr(gamma), head_dim, norm_cols, eps,
         OUT_DTYPES[out_dtype], _ptr(out), out.stride(0), _ptr(device_error), _stream(stream)))
+    return out
+
+
+def nvfp4_gemm_nvfp4_out(a: Nvfp4Tensor, b: Nvfp4Tensor, epilogue: str, out_tensor_scale: torch.Tensor,
+                         bias: Optional[torch.Tensor] = None, gamma: Optional[torch.Tensor] = None,
+                         head_dim: int = 256, norm_cols: int = 0, eps: float = 1e-6,
+                         out: Optional[Nvfp4Tensor] = None, device_error: Optional[torch.Tensor] = None,
+                         stream=None) -> Nvfp4Tensor:
+    """The fused GEMM writing its output as NVFP4 with a static tensor scale (fp32 [1] on the
+    device); the result is an A operand for the next nvfp4_gemm."""
+    assert a.K == b.K
+    assert out_tensor_scale.dtype == torch.float32 and out_tensor_scale.numel() == 1
+    M, N, K = a.rows, b.rows, a.K
+    width = N // 2 if epilogue == "gated_silu" else N
+    if out is None:
+        codes = torch.empty((M, width // 2), dtype=torch.uint8, device=a.codes.device)
+        scales = torch.empty(max(nvfp4_scales_bytes(M, width), 16), dtype=torch.uint8, device=a.codes.device)
+        out = Nvfp4Tensor(codes, scales, out_tensor_scale, M, width)
+    _check("nvfp4_gemm_nvfp4_out", lib().nvfp4_gemm_nvfp4_out(
+        _ptr(a.codes), _ptr(a.scales), _ptr(a.ts), _ptr(b.codes), _ptr(b.scales), _ptr(b.ts),
+        M, N, K, EPILOGUES[epilogue], _ptr(bias), _ptr(gamma), head_dim, norm_cols, eps,
+        _ptr(out_tensor_scale), _ptr(out.codes), _ptr(out.scales), _ptr(device_error), _stream(stream)))
     return out
 
 

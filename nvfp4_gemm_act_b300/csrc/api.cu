@@ -147,14 +147,16 @@ nvfp4_status nvfp4_pack_weights(const void* w, int64_t K, int64_t N, int gated_i
   return from_cuda(cudaMemsetAsync(amax, 0, nvfp4_workspace_bytes(), s));
 }
 
-nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_ts,
-                        const uint8_t* b_codes, const uint8_t* b_scales, const float* b_ts, int64_t M,
-                        int64_t N, int64_t K, nvfp4_epilogue epi, const float* bias, const float* gamma,
-                        int head_dim, int64_t norm_cols, float eps, nvfp4_out_dtype out_dtype, void* out,
-                        int64_t ldo, int* device_error, nvfp4_stream_t stream) {
+namespace {
+
+// Shape / argument checks and argument packing shared by the two GEMM entry points; the
+// output-specific checks are the callers'.
+nvfp4_status gemm_args(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_ts,
+                       const uint8_t* b_codes, const uint8_t* b_scales, const float* b_ts, int64_t M, int64_t N,
+                       int64_t K, nvfp4_epilogue epi, const float* bias, const float* gamma, int head_dim,
+                       int64_t norm_cols, float eps, int* device_error, nvfp4::GemmArgs& a, int64_t& out_cols) {
   if (epi != NVFP4_EPI_BIAS && epi != NVFP4_EPI_HEAD_RMSNORM && epi != NVFP4_EPI_GATED_SILU)
     return NVFP4_ERR_ARG;
-  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_ARG;
   if (epi == NVFP4_EPI_HEAD_RMSNORM) {
     if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256) return NVFP4_ERR_ARG;
     if (!(eps >= 0.0f) || eps != eps) return NVFP4_ERR_ARG;
@@ -163,18 +165,7 @@ nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const f
   if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
   if (epi == NVFP4_EPI_HEAD_RMSNORM && (norm_cols < 0 || norm_cols > N || norm_cols % head_dim != 0))
     return NVFP4_ERR_SHAPE;
-  const int64_t out_cols = epi == NVFP4_EPI_GATED_SILU ? N / 2 : N;
-  if (ldo < out_cols) return NVFP4_ERR_SHAPE;
-  if (M == 0) return NVFP4_OK;  // empty: nothing is read or written (pointers may be NULL)
-  if (a_codes == nullptr || a_scales == nullptr || a_ts == nullptr || b_codes == nullptr ||
-      b_scales == nullptr || b_ts == nullptr || out == nullptr)
-    return NVFP4_ERR_NULL;
-  if (epi == NVFP4_EPI_HEAD_RMSNORM && gamma == nullptr && norm_cols > 0) return NVFP4_ERR_NULL;
-  if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(b_codes) || !aligned16(b_scales) ||
-      !aligned16(out) || ldo % (out_dtype == NVFP4_OUT_BF16 ? 8 : 4) != 0)
-    return NVFP4_ERR_ALIGN;
-  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
-  nvfp4::GemmArgs a;
+  out_cols = epi == NVFP4_EPI_GATED_SILU ? N / 2 : N;
   a.a_codes = a_codes;
   a.a_scales = a_scales;
   a.a_ts = a_ts;
@@ -190,10 +181,72 @@ nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const f
   a.head_dim = epi == NVFP4_EPI_HEAD_RMSNORM ? head_dim : 256;
   a.norm_cols = epi == NVFP4_EPI_HEAD_RMSNORM ? norm_cols : 0;
   a.eps = eps;
+  a.err = device_error;
+  return NVFP4_OK;
+}
+
+// Input pointer checks (after M == 0 has returned).
+nvfp4_status gemm_inputs_ok(const nvfp4::GemmArgs& a) {
+  if (a.a_codes == nullptr || a.a_scales == nullptr || a.a_ts == nullptr || a.b_codes == nullptr ||
+      a.b_scales == nullptr || a.b_ts == nullptr)
+    return NVFP4_ERR_NULL;
+  if (a.epi == NVFP4_EPI_HEAD_RMSNORM && a.gamma == nullptr && a.norm_cols > 0) return NVFP4_ERR_NULL;
+  if (!aligned16(a.a_codes) || !aligned16(a.a_scales) || !aligned16(a.b_codes) || !aligned16(a.b_scales))
+    return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
+}  // namespace
+
+nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_ts,
+                        const uint8_t* b_codes, const uint8_t* b_scales, const float* b_ts, int64_t M,
+                        int64_t N, int64_t K, nvfp4_epilogue epi, const float* bias, const float* gamma,
+                        int head_dim, int64_t norm_cols, float eps, nvfp4_out_dtype out_dtype, void* out,
+                        int64_t ldo, int* device_error, nvfp4_stream_t stream) {
+  nvfp4::GemmArgs a;
+  int64_t out_cols = 0;
+  if (nvfp4_status st = gemm_args(a_codes, a_scales, a_ts, b_codes, b_scales, b_ts, M, N, K, epi, bias, gamma,
+                                  head_dim, norm_cols, eps, device_error, a, out_cols);
+      st != NVFP4_OK)
+    return st;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_ARG;
+  if (ldo < out_cols) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;  // empty: nothing is read or written (pointers may be NULL)
+  if (nvfp4_status st = gemm_inputs_ok(a); st != NVFP4_OK) return st;
+  if (out == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(out) || ldo % (out_dtype == NVFP4_OUT_BF16 ? 8 : 4) != 0) return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
   a.out_fp32 = out_dtype == NVFP4_OUT_FP32 ? 1 : 0;
   a.out = out;
   a.ldo = ldo;
-  a.err = device_error;
+  return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status nvfp4_gemm_nvfp4_out(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_ts,
+                                  const uint8_t* b_codes, const uint8_t* b_scales, const float* b_ts, int64_t M,
+                                  int64_t N, int64_t K, nvfp4_epilogue epi, const float* bias,
+                                  const float* gamma, int head_dim, int64_t norm_cols, float eps,
+                                  const float* out_tensor_scale, uint8_t* out_codes, uint8_t* out_scales,
+                                  int* device_error, nvfp4_stream_t stream) {
+  nvfp4::GemmArgs a;
+  int64_t out_cols = 0;
+  if (nvfp4_status st = gemm_args(a_codes, a_scales, a_ts, b_codes, b_scales, b_ts, M, N, K, epi, bias, gamma,
+                                  head_dim, norm_cols, eps, device_error, a, out_cols);
+      st != NVFP4_OK)
+    return st;
+  if (out_cols % 64 != 0) return NVFP4_ERR_SHAPE;  // the output is the next GEMM's K
+  if (M == 0) return NVFP4_OK;
+  if (nvfp4_status st = gemm_inputs_ok(a); st != NVFP4_OK) return st;
+  if (out_tensor_scale == nullptr || out_codes == nullptr || out_scales == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(out_codes) || !aligned16(out_scales)) return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  a.out_fp32 = 0;
+  a.out = nullptr;
+  a.ldo = out_cols;
+  a.out_nvfp4 = 1;
+  a.out_codes = out_codes;
+  a.out_scales = out_scales;
+  a.out_ts = out_tensor_scale;
   return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -97,7 +97,9 @@ constexpr int kOffEpiBuf = kOffXch + kXchBytes;               // per-warp store 
 constexpr int kEpiBufBytes = 32 * 64;                         // 32 rows x 64 bytes per warp
 constexpr int kOffFlags = kOffEpiBuf + kEpiWarps * kEpiBufBytes;  // epilogue wait results
 static_assert(2 * kEpiWarps * 4 <= 64, "two tiles' epilogue flags");
-constexpr int kOffBar = kOffFlags + 64;
+constexpr int kOffQTab = kOffFlags + 64;                     // NVFP4 output: 1/d and code tables
+constexpr int kQTabBytes = 128 * 4 * 2;
+constexpr int kOffBar = kOffQTab + kQTabBytes;
 constexpr int kBarBytes = 256;
 constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;        // + slack to align to 1 KB
 
@@ -134,6 +136,19 @@ struct EpiParams {
   int norm_cols;
   float eps;
   int out_fp32;
+  // NVFP4 output (codes [M, width/2] + tiled scales, static output tensor scale) instead of
+  // `out`: the bf16-rounded epilogue values are quantized exactly as nvfp4_quantize would
+  int out_nvfp4;
+  uint8_t* out_codes;
+  uint8_t* out_scales;
+  const float* out_ts;
+};
+
+// Shared tables and route of the output tensor scale (NVFP4 output only).
+struct QuantOut {
+  const float* inv_tab;
+  const uint32_t* code_tab;
+  ScaleRoute sr;
 };
 
 // Stores this warp's 32 rows x NV values (thread = row, y[] = its values, columns
@@ -196,6 +211,44 @@ __device__ __forceinline__ void store_rows(const EpiParams& p, const float* y, i
   }
 }
 
+// NVFP4 output of this thread's row (row0 + lane): its NV values y[] are output columns
+// [col0, col0 + NV) (col0 a multiple of 16, NV of 64). Each 16-value block is rounded to bf16
+// and quantized; rows past M (padding of the 128-row scale tiles) get zero scales.
+template <int NV>
+__device__ __forceinline__ void store_rows_nvfp4(const EpiParams& p, const QuantOut& qo, const float* y, int row0,
+                                                 int col0, int width, int lane) {
+  const int row = row0 + lane;
+  const uint32_t gpr = static_cast<uint32_t>(width) >> 6;  // 64-column scale atoms per row band
+  const bool real = row < p.M;
+#pragma unroll
+  for (int b = 0; b < NV / 16; ++b) {
+    const int col = col0 + b * 16;
+    if (col >= width) break;
+    const float* v = y + b * 16;
+    const uint4 lo = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                pack_bf16x2(v[6], v[7]));
+    const uint4 hi = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                                pack_bf16x2(v[14], v[15]));
+    uint32_t stored = 0u;
+    if (real) {
+      uint2 c;
+      stored = quantize_block(lo, hi, qo.sr, qo.inv_tab, qo.code_tab, c);
+      *reinterpret_cast<uint2*>(p.out_codes + (int64_t)row * (width >> 1) + (col >> 1)) = c;
+    }
+    p.out_scales[scale_offset(static_cast<uint32_t>(row), static_cast<uint32_t>(col >> 4), gpr)] =
+        static_cast<uint8_t>(stored);
+  }
+}
+
+template <int NV>
+__device__ __forceinline__ void store_out(const EpiParams& p, const QuantOut& qo, const float* y, int row0,
+                                          int col0, int width, uint32_t buf, int lane) {
+  if (p.out_nvfp4)
+    store_rows_nvfp4<NV>(p, qo, y, row0, col0, width, lane);
+  else
+    store_rows<NV>(p, y, row0, col0, width, buf, lane);
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) {
   // sigma(g) = 1 / (1 + e^-g); __fdividef returns 0 once the denominator exceeds 2^126
   return g * __fdividef(1.0f, 1.0f + __expf(-g)) * u;
@@ -203,14 +256,14 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 // Epilogue of one thread: its row's 128 columns [c0, c0 + 128) of the tile, already in z
 // (z = alpha * acc + bias). `xch` is the shared half-row exchange (RMSNorm, head 256).
-__device__ __forceinline__ void epilogue_row(const EpiParams& p, float (&z)[kHalf], int row0, int c0,
-                                             int half, int row_local, const float* gamma_s, float* xch,
+__device__ __forceinline__ void epilogue_row(const EpiParams& p, const QuantOut& qo, float (&z)[kHalf], int row0,
+                                             int c0, int half, int row_local, const float* gamma_s, float* xch,
                                              uint32_t buf, int lane) {
   if (p.epi == NVFP4_EPI_GATED_SILU) {
     float y[kHalf / 2];
 #pragma unroll
     for (int j = 0; j < kHalf / 2; ++j) y[j] = silu_mul(z[2 * j], z[2 * j + 1]);
-    store_rows<kHalf / 2>(p, y, row0, c0 >> 1, p.N >> 1, buf, lane);
+    store_out<kHalf / 2>(p, qo, y, row0, c0 >> 1, p.N >> 1, buf, lane);
     return;
   }
   if (p.epi == NVFP4_EPI_HEAD_RMSNORM) {
@@ -250,7 +303,7 @@ __device__ __forceinline__ void epilogue_row(const EpiParams& p, float (&z)[kHal
       }
     }
   }
-  store_rows<kHalf>(p, z, row0, c0, p.N, buf, lane);
+  store_out<kHalf>(p, qo, z, row0, c0, p.N, buf, lane);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -455,6 +508,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xch = reinterpret_cast<float*>(smem + kOffXch);
     volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
     const float alpha = __fmul_rn(__ldg(ep.a_ts), __ldg(ep.b_ts));
+    QuantOut qo;
+    {
+      float* inv_tab = reinterpret_cast<float*>(smem + kOffQTab);
+      uint32_t* code_tab = reinterpret_cast<uint32_t*>(smem + kOffQTab + 512);
+      qo.inv_tab = inv_tab;
+      qo.code_tab = code_tab;
+      const float ts_o = ep.out_nvfp4 ? __ldg(ep.out_ts) : 0.0f;
+      qo.sr = scale_route(ts_o);
+      if (ep.out_nvfp4 && et < 128) build_scale_table_entry(static_cast<uint32_t>(et), ts_o, inv_tab, code_tab);
+      // (the first tile's epilogue-wide barrier orders the tables before any use)
+    }
     const bool gated = ep.epi == NVFP4_EPI_GATED_SILU;
     const int nhalf = ep.N >> 1;
     uint32_t it = 0;
@@ -509,8 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* bh = bias_s + half * kHalf;
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) z[i] = fmaf(alpha, z[i], bh[i]);
-      epilogue_row(ep, z, m_blk * kBM + q * 32, n_base + half * kHalf, half, row_local, gamma_s + half * kHalf,
-                   xch, sbase + kOffEpiBuf + ew * kEpiBufBytes, lane);
+      epilogue_row(ep, qo, z, m_blk * kBM + q * 32, n_base + half * kHalf, half, row_local,
+                   gamma_s + half * kHalf, xch, sbase + kOffEpiBuf + ew * kEpiBufBytes, lane);
     }
   }
 
@@ -598,6 +662,10 @@ nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   ep.norm_cols = static_cast<int>(a.norm_cols);
   ep.eps = a.eps;
   ep.out_fp32 = a.out_fp32;
+  ep.out_nvfp4 = a.out_nvfp4;
+  ep.out_codes = a.out_codes;
+  ep.out_scales = a.out_scales;
+  ep.out_ts = a.out_ts;
   const int num_m = static_cast<int>((a.M + kBM - 1) / kBM);
   const int num_n = static_cast<int>((a.N + kBN - 1) / kBN);
   const int num_pair_tiles = ((num_m + kCluster - 1) / kCluster) * num_n;

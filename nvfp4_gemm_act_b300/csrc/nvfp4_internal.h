@@ -50,6 +50,11 @@ struct GemmArgs {
   void* out;
   int64_t ldo;
   int* err;
+  // NVFP4 output instead of `out` (codes [M, out_cols/2], tiled scales, static tensor scale)
+  int out_nvfp4 = 0;
+  uint8_t* out_codes = nullptr;
+  uint8_t* out_scales = nullptr;
+  const float* out_ts = nullptr;
 };
 
 // Validated arguments in, kernel launched (or an error code out).

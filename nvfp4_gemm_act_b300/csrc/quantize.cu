@@ -19,7 +19,6 @@ namespace nvfp4 {
 namespace {
 
 constexpr float kTsDivisor = 2688.0f;        // 6 (E2M1 max) * 448 (E4M3 max)
-constexpr float kFltMin = 1.17549435082e-38f;  // 2^-126
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 v;
@@ -56,18 +55,6 @@ __device__ __forceinline__ BlockScale block_scale(float bamax, float ts, float s
   r.code = r.live ? code : 0u;
   r.inv = r.live ? __fdiv_rn(1.0f, d) : 0.0f;
   return r;
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// 8 bf16 values (in memory order) -> 4 bytes of E2M1 codes, element 2j in the low nibble.
-__device__ __forceinline__ uint32_t encode8(const uint4& v, float inv) {
-  const uint32_t b0 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.x), inv), __fmul_rn(bf16_hi(v.x), inv));
-  const uint32_t b1 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.y), inv), __fmul_rn(bf16_hi(v.y), inv));
-  const uint32_t b2 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.z), inv), __fmul_rn(bf16_hi(v.z), inv));
-  const uint32_t b3 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.w), inv), __fmul_rn(bf16_hi(v.w), inv));
-  return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -144,77 +131,6 @@ __global__ void __launch_bounds__(kAmaxThreads)
 constexpr int kQuantThreads = 256;
 constexpr int kQuantUnroll = 4;
 
-// max(|a|, |b|) per bf16 lane (the sign of the result is discarded by the caller).
-__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// |bf16| maximum of the 16 values in lo, hi, as the fp32 value (exact).
-__device__ __forceinline__ float absmax16(const uint4& lo, const uint4& hi) {
-  const uint32_t m = bf16x2_max_abs(bf16x2_max_abs(bf16x2_max_abs(lo.x, lo.y), bf16x2_max_abs(lo.z, lo.w)),
-                                    bf16x2_max_abs(bf16x2_max_abs(hi.x, hi.y), bf16x2_max_abs(hi.z, hi.w)));
-  const uint32_t h = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
-  return __uint_as_float(h << 16);
-}
-
-// Tables of one tensor scale, built by threads 0..127 (caller synchronises): fp32(1 / d) and
-// the stored code for each E4M3 code s, d = fp32(dec(s) ts); zero entries for a zero block.
-// Code 127 is E4M3 NaN (never produced by the saturating conversion).
-__device__ __forceinline__ void build_scale_tables(float ts, float* inv_tab, uint32_t* code_tab) {
-  if (threadIdx.x < 128) {
-    const uint32_t c = threadIdx.x;
-    const float d = __fmul_rn(e4m3_to_f32(c), ts);
-    const bool live = ts > 0.0f && c < 127u && d >= kFltMin;
-    inv_tab[c] = live ? __fdiv_rn(1.0f, d) : 0.0f;
-    code_tab[c] = live ? c : 0u;
-  }
-}
-
-struct ScaleRoute {
-  float six_ts;
-  float rcp_six_ts;
-  bool fast;  // 1 / (6 ts) finite and normal: the reciprocal route applies
-};
-
-__device__ __forceinline__ ScaleRoute scale_route(float ts) {
-  ScaleRoute r;
-  r.six_ts = __fmul_rn(6.0f, ts);
-  r.fast = r.six_ts >= 0x1p-125f && r.six_ts <= 0x1p125f;
-  r.rcp_six_ts = r.fast ? __frcp_rn(r.six_ts) : 0.0f;
-  return r;
-}
-
-// One 16-element block (lo: elements 0-7, hi: 8-15): its 8 code bytes; returns the stored
-// scale code (0 for a zero block, whose codes are +0).
-__device__ __forceinline__ uint32_t quantize_block(const uint4& lo, const uint4& hi, const ScaleRoute& sr,
-                                                   const float* inv_tab, const uint32_t* code_tab, uint2& out) {
-  const float bamax = absmax16(lo, hi);
-  uint32_t s;
-  if (sr.fast) {
-    const float qa = __fmul_rn(bamax, sr.rcp_six_ts);
-    const uint32_t s_lo = cvt_e4m3(__fmul_rn(qa, 1.0f - 0x1p-20f));
-    const uint32_t s_hi = cvt_e4m3(__fmul_rn(qa, 1.0f + 0x1p-20f));
-    s = s_lo == s_hi ? s_lo : cvt_e4m3(__fdiv_rn(bamax, sr.six_ts));
-  } else {
-    s = cvt_e4m3(__fdiv_rn(bamax, sr.six_ts));
-  }
-  s &= 127u;
-  const uint32_t stored = code_tab[s];
-  out = make_uint2(0u, 0u);
-  if (stored != 0u) {
-    const float inv = inv_tab[s];
-    out = make_uint2(encode8(lo, inv), encode8(hi, inv));
-  }
-  return stored;
-}
-
-// Byte offset of the scale of (row r, 16-element block kb) in the tiled scale layout.
-__device__ __forceinline__ uint32_t scale_offset(uint32_t r, uint32_t kb, uint32_t gpr) {
-  return ((r >> 7) * gpr + (kb >> 2)) * 512u + (r & 31u) * 16u + ((r >> 5) & 3u) * 4u + (kb & 3u);
-}
-
 template <bool kLoad32>  // one 32-byte load per lane (x 32-byte aligned, ldx % 16 == 0)
 __global__ void __launch_bounds__(kQuantThreads, 4)
     quantize_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M,
@@ -227,7 +143,7 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
                        ? *ts_in
                        : __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile unsigned*>(ws)), kTsDivisor);
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
-  build_scale_tables(ts, inv_tab, code_tab);
+  if (threadIdx.x < 128) build_scale_table_entry(threadIdx.x, ts, inv_tab, code_tab);
   const ScaleRoute sr = scale_route(ts);
   __syncthreads();
 
@@ -382,7 +298,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     while (!(all_in = ld_acquire_gpu(ws + 1) >= gridDim.x)) {
       if (global_timer_ns() - t0 > timeout_ns) break;
     }
-    __threadfence();
+    // (the acquire loads order the reads below after every CTA's release)
     const bool bad = !all_in || ld_acquire_gpu(ws + 3) != 0u;
     const uint32_t amax_bits = ld_acquire_gpu(ws);
     failed = bad ? 1 : 0;
@@ -392,7 +308,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const float ts = ts_s;
   if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
   if (!failed) {
-    build_scale_tables(ts, inv_tab, code_tab);
+    if (threadIdx.x < 128) build_scale_table_entry(threadIdx.x, ts, inv_tab, code_tab);
     const ScaleRoute sr = scale_route(ts);
     __syncthreads();
     // quantize: item = (row, 512-element chunk); lane = one 16-element block of the chunk;

@@ -113,6 +113,30 @@ def test_gemm_host_checks():
     assert g(M=0, ac=None) == OK
 
 
+def gq(**kw):
+    a = dict(ac=FAKE, asc=FAKE, ats=FAKE, bc=FAKE, bsc=FAKE, bts=FAKE, M=128, N=256, K=256, epi=0,
+             bias=None, gamma=None, hd=256, nc=0, eps=1e-6, ots=FAKE, oc=FAKE, osc=FAKE, err=None)
+    a.update(kw)
+    return nv.lib().nvfp4_gemm_nvfp4_out(a["ac"], a["asc"], a["ats"], a["bc"], a["bsc"], a["bts"], a["M"],
+                                         a["N"], a["K"], a["epi"], a["bias"], a["gamma"], a["hd"], a["nc"],
+                                         a["eps"], a["ots"], a["oc"], a["osc"], a["err"], None)
+
+
+def test_gemm_nvfp4_out_host_checks():
+    assert gq(N=32) == ERR_SHAPE                   # output width % 64
+    assert gq(epi=2, N=64) == ERR_SHAPE            # gated output width N/2 = 32
+    assert gq(epi=2, N=128) != ERR_SHAPE
+    assert gq(ots=None) == ERR_NULL
+    assert gq(oc=None) == ERR_NULL
+    assert gq(osc=None) == ERR_NULL
+    assert gq(ac=None) == ERR_NULL
+    assert gq(oc=FAKE + 8) == ERR_ALIGN
+    assert gq(epi=5) == ERR_ARG
+    assert gq(K=96) == ERR_SHAPE
+    assert gq(M=0) == OK
+    assert gq(M=0, oc=None, ots=None) == OK
+
+
 def test_pack_host_checks():
     L = nv.lib()
     assert L.nvfp4_pack_weights(None, 256, 256, 0, FAKE, FAKE, FAKE, FAKE, None) == ERR_NULL
