@@ -50,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-rows", type=int, default=16, help="oracle rows sampled per GEMM")
     p.add_argument("--only", choices=["qkv_rmsnorm", "gated_up", "down_bias"], default=None,
                    help="run one of the three layers only (for profiler captures)")
+    p.add_argument("--chain", action="store_true",
+                   help="up-projection -> down-projection at M=4608: fused NVFP4 output vs bf16 + quantize")
     p.add_argument("--sweep", action="store_true",
                    help="batch sweep: one JSON line per (M, GEMM), M in 512..18432")
     return p.parse_args(argv)
@@ -581,9 +583,68 @@ def run_sweep(args):
                           "quantize_gbs": round(qbytes / (qms / 1e3) / 1e9, 1)}), flush=True)
 
 
+def run_chain(args):
+    """The up-projection (gated SiLU) feeding the down-projection at M=4608, three ways: the up
+    GEMM writing NVFP4 for the down GEMM (static scale); the up GEMM writing bf16, then the
+    quantizer with the same static scale; bf16, then the quantizer with a dynamic scale. The
+    static scale is calibrated once, before timing, from the bf16 output's amax. Each variant
+    starts from the quantized up-projection input; L2 is flushed before every timed chain."""
+    import torch
+
+    import nvfp4_gemm_act_b300 as nv
+    from nvfp4_gemm_act_b300 import workloads as W
+    dev = "cuda:0"
+    up, down = W.GATED_UP, W.DOWN_BIAS
+    assert up.out_cols == down.K
+    qa = nv.nvfp4_quantize(W.make_x(up).to(dev))
+    qb_up = nv.nvfp4_pack_weights(W.make_w(up).to(dev), gated_interleave=True)
+    qb_dn = nv.nvfp4_pack_weights(W.make_w(down).to(dev))
+    bias_dn = W.make_bias(down).to(dev)
+    y_mid = nv.nvfp4_gemm(qa, qb_up, up.epilogue)
+    ts_mid = (y_mid.float().abs().max() / 2688.0).reshape(1).contiguous()
+    q_mid = nv._alloc_nvfp4(up.M, up.out_cols, dev)
+    ws = torch.zeros(16, dtype=torch.uint8, device=dev)
+    out = torch.empty((down.M, down.out_cols), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def fused():
+        m = nv.nvfp4_gemm_nvfp4_out(qa, qb_up, up.epilogue, ts_mid, out=q_mid)
+        nv.nvfp4_gemm(m, qb_dn, down.epilogue, bias=bias_dn, out=out)
+
+    def unfused(static):
+        nv.nvfp4_gemm(qa, qb_up, up.epilogue, out=y_mid)
+        m = nv.nvfp4_quantize(y_mid, out=q_mid, tensor_scale_in=ts_mid if static else None, workspace=ws)
+        nv.nvfp4_gemm(m, qb_dn, down.epilogue, bias=bias_dn, out=out)
+
+    variants = {"fused_nvfp4_out": fused, "bf16_then_quantize_static": lambda: unfused(True),
+                "bf16_then_quantize_dynamic": lambda: unfused(False)}
+    res = {}
+    for name, fn in variants.items():
+        ts = []
+        for it in range(max(args.warmup, 3) + args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= max(args.warmup, 3):
+                ts.append(e0.elapsed_time(e1))
+        res[name] = round(float(np.median(ts)), 5)
+    flops = up.flops + down.flops
+    print(json.dumps({"chain": "up-projection (gated SiLU) -> down-projection, M=4608", "ms": res,
+                      "tflops": {k: round(flops / (v / 1e3) / 1e12, 1) for k, v in res.items()},
+                      "intermediate_bf16_mb": round(up.M * up.out_cols * 2 / 1e6, 1),
+                      "intermediate_nvfp4_mb": round(up.M * up.out_cols * (0.5 + 1 / 16) / 1e6, 1),
+                      "steps": args.steps}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
+    if args.chain:
+        run_chain(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
