@@ -46,6 +46,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "nvfp4_device.cuh"
@@ -153,20 +154,25 @@ struct QuantOut {
 
 // Stores this warp's 32 rows x NV values (thread = row, y[] = its values, columns
 // [col0, col0 + NV) of the output) through the warp's 2 KB shared buffer: each lane writes
-// its row's next 64 bytes (16-byte pieces XOR-swizzled by row pair, so the row-per-lane
-// writes hit distinct banks), then each global store instruction writes 8 rows x 64
-// contiguous bytes instead of 32 scattered 16-byte pieces.
+// its row's next 64 bytes (16-byte pieces XOR-swizzled by row pair -- the TMA's 64-byte
+// swizzle -- so the row-per-lane writes hit distinct banks), then one lane hands the 32 x 64
+// byte box to the TMA. The warp issues no global stores of its own, and the memory
+// instructions it does issue are a third of a read-back-and-store scheme's.
 template <int NV>
-__device__ __forceinline__ void store_rows(const EpiParams& p, const float* y, int row0, int col0,
-                                           int width, uint32_t buf, int lane) {
+__device__ __forceinline__ void store_rows(const EpiParams& p, const void* tm_out, const float* y, int row0,
+                                           int col0, int width, uint32_t buf, int lane) {
+  if (row0 >= p.M) return;  // the warp's 32 rows all lie past M (uniform across the warp)
   const bool bf16 = !p.out_fp32;
-  const int per_chunk = bf16 ? 32 : 16;  // values per 64-byte row segment
   const int swz_w = (lane >> 1) & 3;
 #pragma unroll
   for (int c = 0; c < NV; c += 16) {
+    if (bf16 && (c & 31) != 0) continue;  // bf16 chunks are 32 values; handled at c % 32 == 0
+    if (col0 + c >= width) break;         // past a ragged last tile's columns
+    // the TMA has finished reading the buffer's previous box
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
     // write: 64 bytes of this lane's row (bf16: 32 values; fp32: 16 values)
     if (bf16) {
-      if ((c & 31) != 0) continue;  // bf16 chunks are 32 values; handled at c % 32 == 0
 #pragma unroll
       for (int piece = 0; piece < 4; ++piece) {
         const float* v = y + c + piece * 8;
@@ -186,28 +192,13 @@ __device__ __forceinline__ void store_rows(const EpiParams& p, const float* y, i
                      : "memory");
       }
     }
+    fence_proxy_async_smem();  // this lane's writes, visible to the TMA
     __syncwarp();
-    // read back row-contiguous and store: lane -> (row r = i * 8 + lane / 4, piece lane % 4)
-    const int piece = lane & 3;
-    const int col = col0 + c + piece * (bf16 ? 8 : 4);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = i * 8 + (lane >> 2);
-      uint4 w;
-      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
-                   : "r"(buf + r * 64 + ((piece ^ ((r >> 1) & 3)) * 16))
-                   : "memory");
-      const int row = row0 + r;
-      if (row < p.M && col < width) {
-        if (bf16)
-          *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + (int64_t)row * p.ldo + col) = w;
-        else
-          *reinterpret_cast<uint4*>(static_cast<float*>(p.out) + (int64_t)row * p.ldo + col) = w;
-      }
+    if (lane == 0) {
+      // rows past M and columns past the width are clipped by the tensor map
+      tma_store_2d(tm_out, buf, col0 + c, row0);
+      bulk_commit_group();
     }
-    __syncwarp();
-    (void)per_chunk;
   }
 }
 
@@ -241,12 +232,12 @@ __device__ __forceinline__ void store_rows_nvfp4(const EpiParams& p, const Quant
 }
 
 template <int NV>
-__device__ __forceinline__ void store_out(const EpiParams& p, const QuantOut& qo, const float* y, int row0,
-                                          int col0, int width, uint32_t buf, int lane) {
+__device__ __forceinline__ void store_out(const EpiParams& p, const QuantOut& qo, const void* tm_out, const float* y,
+                                          int row0, int col0, int width, uint32_t buf, int lane) {
   if (p.out_nvfp4)
     store_rows_nvfp4<NV>(p, qo, y, row0, col0, width, lane);
   else
-    store_rows<NV>(p, y, row0, col0, width, buf, lane);
+    store_rows<NV>(p, tm_out, y, row0, col0, width, buf, lane);
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
@@ -256,14 +247,14 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 
 // Epilogue of one thread: its row's 128 columns [c0, c0 + 128) of the tile, already in z
 // (z = alpha * acc + bias). `xch` is the shared half-row exchange (RMSNorm, head 256).
-__device__ __forceinline__ void epilogue_row(const EpiParams& p, const QuantOut& qo, float (&z)[kHalf], int row0,
-                                             int c0, int half, int row_local, const float* gamma_s, float* xch,
-                                             uint32_t buf, int lane) {
+__device__ __forceinline__ void epilogue_row(const EpiParams& p, const QuantOut& qo, const void* tm_out,
+                                             float (&z)[kHalf], int row0, int c0, int half, int row_local,
+                                             const float* gamma_s, float* xch, uint32_t buf, int lane) {
   if (p.epi == NVFP4_EPI_GATED_SILU) {
     float y[kHalf / 2];
 #pragma unroll
     for (int j = 0; j < kHalf / 2; ++j) y[j] = silu_mul(z[2 * j], z[2 * j + 1]);
-    store_out<kHalf / 2>(p, qo, y, row0, c0 >> 1, p.N >> 1, buf, lane);
+    store_out<kHalf / 2>(p, qo, tm_out, y, row0, c0 >> 1, p.N >> 1, buf, lane);
     return;
   }
   if (p.epi == NVFP4_EPI_HEAD_RMSNORM) {
@@ -303,13 +294,14 @@ __device__ __forceinline__ void epilogue_row(const EpiParams& p, const QuantOut&
       }
     }
   }
-  store_out<kHalf>(p, qo, z, row0, c0, p.N, buf, lane);
+  store_out<kHalf>(p, qo, tm_out, z, row0, c0, p.N, buf, lane);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                       const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
-                      int K, int num_m_blocks, int num_tiles, EpiParams ep, int* err, uint64_t timeout_ns) {
+                      const __grid_constant__ CUtensorMap tm_out, int K, int num_m_blocks, int num_tiles,
+                      EpiParams ep, int* err, uint64_t timeout_ns) {
   // num_tiles counts pair tiles: (row-tile pair, weight tile); row pairs fastest.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -342,6 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_b);
     prefetch_tmap(&tm_sfa);
     prefetch_tmap(&tm_sfb);
+    if (!ep.out_nvfp4) prefetch_tmap(&tm_out);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 2);            // the leader's two producers' arrivals (+ both CTAs' bytes)
       mbar_init(empty_bar(s), 1);           // the leader's MMA commit
@@ -573,9 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* bh = bias_s + half * kHalf;
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) z[i] = fmaf(alpha, z[i], bh[i]);
-      epilogue_row(ep, qo, z, m_blk * kBM + q * 32, n_base + half * kHalf, half, row_local,
+      epilogue_row(ep, qo, &tm_out, z, m_blk * kBM + q * 32, n_base + half * kHalf, half, row_local,
                    gamma_s + half * kHalf, xch, sbase + kOffEpiBuf + ew * kEpiBufBytes, lane);
     }
+    // the warp's tile stores have completed (their sources are this CTA's shared memory)
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -631,12 +627,32 @@ bool encode_scales_map(CUtensorMap* map, const void* base, int64_t rows, int64_t
 
 }  // namespace
 
+// The output [M, width] (row stride ldo elements) in boxes of 32 rows x 64 bytes with the
+// 64-byte swizzle of the epilogue's staging buffers.
+bool encode_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t width, int64_t ldo, bool fp32) {
+  auto fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  const int64_t elem = fp32 ? 4 : 2;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldo * elem)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / elem), 32u};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
-  CUtensorMap tm_a, tm_b, tm_sfa, tm_sfb;
+  CUtensorMap tm_a, tm_b, tm_sfa, tm_sfb, tm_out;
   if (!encode_codes_map(&tm_a, a.a_codes, a.M, a.K, kBM)) return NVFP4_ERR_LAUNCH;
   if (!encode_codes_map(&tm_b, a.b_codes, a.N, a.K, kBRowsPerCta)) return NVFP4_ERR_LAUNCH;
   if (!encode_scales_map(&tm_sfa, a.a_scales, a.M, a.K)) return NVFP4_ERR_LAUNCH;
   if (!encode_scales_map(&tm_sfb, a.b_scales, a.N, a.K)) return NVFP4_ERR_LAUNCH;
+  const int64_t width = a.epi == NVFP4_EPI_GATED_SILU ? a.N / 2 : a.N;
+  if (a.out_nvfp4)
+    std::memset(&tm_out, 0, sizeof(tm_out));  // unused: the NVFP4 output is stored directly
+  else if (!encode_out_map(&tm_out, a.out, a.M, width, a.ldo, a.out_fp32 != 0))
+    return NVFP4_ERR_LAUNCH;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -693,7 +709,7 @@ nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   }();
   const int clusters = std::max(1, std::min(num_pair_tiles, max_clusters));
   cfg.gridDim = dim3(clusters * kCluster, 1, 1);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, tm_a, tm_b, tm_sfa, tm_sfb,
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, tm_a, tm_b, tm_sfa, tm_sfb, tm_out,
                                            static_cast<int>(a.K), num_m, num_pair_tiles, ep, a.err,
                                            wait_timeout_ns());
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH;
