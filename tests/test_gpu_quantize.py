@@ -212,3 +212,27 @@ def test_scale_rounding_boundaries_dynamic_scale(k):
     x = _bf16(xb)
     q = quant_both(x, what=f"E4M3 boundaries, dynamic ts, k={k}")
     assert np.float32(6.0) * gpu_nvfp4_to_np(q)[2] == np.float32(2.0 ** k)
+
+
+def test_large_ragged_strided_dynamic_scale():
+    # X of 1300 x 12288 (32 MB: too large for the SMs' shared memory, so the amax and quantize
+    # passes run as two launches); ragged M (108 padding rows of scale tiles, which must come
+    # out zero from an uninitialised buffer) and a row pitch of 12352 elements
+    w = W.DOWN_BIAS.with_m(1300, seed=91)
+    x = W.make_x(w)
+    big = torch.zeros(1300, 12288 + 64, dtype=torch.bfloat16)
+    big[:, :12288] = x
+    view = big.to(DEV)[:, :12288]
+    q = nv.nvfp4_quantize(view)
+    gc, gs, gt = gpu_nvfp4_to_np(q)
+    xn = to_np_f32(x)
+    ts = R.tensor_scale_ref(xn)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 1279, 1280, 1299],
+                                     np.random.default_rng(92).integers(0, 1300, 25)]))
+    rc, rs, _ = R.quantize_ref(xn[rows], ts)
+    assert_quant_equal((gc[rows], gs[rows], gt), (rc, rs, ts), "large ragged strided")
+    buf = q.scales.cpu().numpy()
+    used = np.zeros(buf.size, bool)
+    r, kb = np.meshgrid(np.arange(1300), np.arange(12288 // 16), indexing="ij")
+    used[R.scale_offset(r, kb, 12288)] = True
+    assert not buf[~used].any(), "padding rows of the scale tiles must be zero"
