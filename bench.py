@@ -52,6 +52,8 @@ def parse_args(argv=None):
                    help="run one of the three layers only (for profiler captures)")
     p.add_argument("--chain", action="store_true",
                    help="up-projection -> down-projection at M=4608: fused NVFP4 output vs bf16 + quantize")
+    p.add_argument("--dit-block", action="store_true",
+                   help="one DiT block's linears chained at 4608 tokens: per-stage CUDA-event times")
     p.add_argument("--sweep", action="store_true",
                    help="batch sweep: one JSON line per (M, GEMM), M in 512..18432")
     return p.parse_args(argv)
@@ -639,9 +641,63 @@ def run_chain(args):
                       "steps": args.steps}), flush=True)
 
 
+def run_dit_block(args):
+    """One DiT block at 4608 tokens (hidden 3072, 12 heads of 256, MLP 12288): the up-projection's
+    static output scale calibrated once from its bf16 output, then per step (L2 flushed first)
+    the whole block with a CUDA-event pair around each stage. One JSON line: median ms per stage
+    (a stage's time includes its activation quantize), its share, and the GEMM rate."""
+    import torch
+
+    from nvfp4_gemm_act_b300.dit_block import STAGES, seeded_dit_block
+    dev = "cuda:0"
+    M = 4608
+    blk, x = seeded_dit_block(M, dev)
+    blk.calibrate(x)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    times = {}
+    total = []
+    sampler = ClockSampler(0)
+
+    def one(t):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        y = blk(x, timings=t)
+        e1.record()
+        torch.cuda.synchronize()
+        return y, e0.elapsed_time(e1)
+
+    for _ in range(max(args.warmup, 3)):
+        one(None)
+    with sampler:
+        for _ in range(args.steps):
+            t = {}
+            y, ms_total = one(t)
+            for k, v in t.items():
+                times.setdefault(k, []).extend(v)
+            total.append(ms_total)
+    assert bool(torch.isfinite(y.float()).all())
+    h, m = blk.hidden, blk.mlp
+    flops = {"qkv_rmsnorm": 2 * M * h * 3 * h, "attention": 4 * M * M * h, "out_proj": 2 * M * h * h,
+             "up_gated_silu": 2 * M * h * 2 * m, "down": 2 * M * m * h}
+    ms = {k: round(float(np.median(times[k])), 5) for k in STAGES}
+    tot = float(np.median(total))
+    print(json.dumps({"dit_block": f"M={M} hidden={h} heads={blk.heads}x{blk.head_dim} mlp={m}",
+                      "total_ms": round(tot, 5), "ms": ms,
+                      "share": {k: round(v / sum(ms.values()), 4) for k, v in ms.items()},
+                      "tflops": {k: round(flops[k] / (ms[k] / 1e3) / 1e12, 1) for k in STAGES},
+                      "nvfp4_gemm_tflops_block": round(blk.gemm_flops(M) / ((tot - ms["attention"]) / 1e3) / 1e12, 1),
+                      "attention": "torch scaled_dot_product_attention, bf16",
+                      "steps": args.steps, "l2": "flushed before each block",
+                      "clocks": sampler.summary()}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
+    if args.dit_block:
+        run_dit_block(args)
+        return
     if args.chain:
         run_chain(args)
         return

@@ -16,6 +16,11 @@ Shapes follow a FLUX-class DiT block (hidden 3072, MLP 12288, 12 heads x head_di
   down_bias       X [4608, 12288] ~ 0.5 * Student-t(df=3); W [12288, 3072] ~ N(0, 0.02);
                   bias N(0, 0.01)
 
+One DiT block chains four linears (attention between the first two): qkv_rmsnorm ->
+attention -> out_proj (W [3072, 3072] ~ N(0, 0.02), bias N(0, 0.01), seed 5) -> gated_up ->
+down_bias. The block's input is qkv_rmsnorm's X; every later layer takes the previous
+stage's output, so only the weights, biases and gain of those layers are drawn.
+
 Every array is drawn in fp64 from ``numpy.random.default_rng((seed, stream))`` (stream 0:
 X, 1: W, 2: bias, 3: gamma, 4: outlier channels; all but X use the layer's seed,
 which ``with_m`` keeps when it reseeds the activations) and rounded to bf16 (X, W) or fp32
@@ -73,7 +78,28 @@ QKV_RMSNORM = Workload("qkv_rmsnorm", 4608, 3072, 9216, EPI_HEAD_RMSNORM, seed=2
 GATED_UP = Workload("gated_up", 4608, 3072, 24576, EPI_GATED_SILU, seed=3, bias_std=None)
 DOWN_BIAS = Workload("down_bias", 4608, 12288, 3072, EPI_BIAS, seed=4, x_dist="student_t")
 
+OUT_PROJ = Workload("out_proj", 4608, 3072, 3072, EPI_BIAS, seed=5)
+
 WORKLOADS = {w.name: w for w in (TINY_BIAS, QKV_RMSNORM, GATED_UP, DOWN_BIAS)}
+
+# One DiT block's linears in order; the 12 attention heads of 256 sit between the first two.
+DIT_BLOCK = (QKV_RMSNORM, OUT_PROJ, GATED_UP, DOWN_BIAS)
+DIT_HEADS = 12
+
+
+def dit_block(M: int = 4608, seed: Optional[int] = None, heads: int = DIT_HEADS, mlp: int = 12288):
+    """The block's four layers on M tokens (`seed` reseeds the block input). Fewer heads or a
+    narrower MLP give a smaller block of the same structure (head_dim 256 throughout), its
+    weights drawn from the same seeds at the smaller shapes."""
+    h = heads * QKV_RMSNORM.head_dim
+    shapes = ((h, 3 * h, 2 * h), (h, h, 0), (h, 2 * mlp, 0), (mlp, h, 0))
+    out = []
+    for i, (w, (K, N, norm_cols)) in enumerate(zip(DIT_BLOCK, shapes)):
+        w = w.with_m(M, seed if i == 0 else None)
+        if (K, N) != (w.K, w.N):
+            w = dataclasses.replace(w, K=K, N=N, norm_cols=norm_cols, name=f"{w.name}_h{h}")
+        out.append(w)
+    return tuple(out)
 
 # Batch sweep: the three DiT GEMMs at M in {512, 1024, 4608, 9216, 18432}; activations of
 # the i-th size drawn with seed 10 + i, each layer keeping its weights.

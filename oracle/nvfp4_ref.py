@@ -371,3 +371,82 @@ def bf16_ulp(y: np.ndarray) -> np.ndarray:
     y = np.asarray(y, np.float64)
     _, e = np.frexp(np.where(y == 0, 1.0, y))
     return np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
+
+
+# ----------------------------------------------------------------------------------------
+# One DiT block's linears chained, attention between the first two.
+# ----------------------------------------------------------------------------------------
+
+def attention_ref(q, k, v) -> np.ndarray:
+    """Scaled dot-product attention per head, every query over every key, fp64.
+
+    q, k, v: [heads, M, d]. out[h, i] = sum_j p[h, i, j] v[h, j] with
+    p[h, i, :] = softmax_j(q[h, i] . k[h, j] / sqrt(d)). The pages name attention as the other
+    large op of the transformer's pass without defining it; this is the textbook form with no
+    mask (all tokens of a DiT block see each other). Subtracting a row's largest score before
+    exp leaves p unchanged and keeps exp finite.
+    """
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    out = np.empty((q.shape[0], q.shape[1], v.shape[2]))
+    for h in range(q.shape[0]):
+        s = (q[h] @ k[h].T) / np.sqrt(q.shape[2])
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        out[h] = (p / p.sum(axis=1, keepdims=True)) @ v[h]
+    return out
+
+
+def _linear_ref(x, w, bias, epilogue, quantized, gamma=None, head_dim=256, norm_cols=0, eps=1e-6,
+                tensor_scale=None):
+    """One linear layer of the block: quantized, the layer as the NVFP4 path defines it (x and
+    W quantized with their own amax scales unless ``tensor_scale`` fixes x's; fp64 GEMM and
+    epilogue); not quantized, the exact fp64 layer epilogue(x @ W + bias)."""
+    kw = dict(bias=bias, gamma=gamma, head_dim=head_dim, norm_cols=norm_cols, eps=eps)
+    if quantized:
+        a = quantize_ref(x, tensor_scale)
+        b = pack_weights_ref(w, gated_interleave=(epilogue == EPI_GATED_SILU))
+        return gemm_ref(*a, *b, epilogue, **kw)
+    c = np.asarray(x, np.float64) @ np.asarray(w, np.float64)
+    if bias is not None:
+        c = c + np.asarray(bias, np.float64)[None, :]
+    if epilogue == EPI_BIAS:
+        return c
+    if epilogue == EPI_HEAD_RMSNORM:
+        return head_rmsnorm_ref(c, gamma, head_dim, norm_cols, eps)
+    return gated_silu_ref(c)
+
+
+def dit_block_ref(x, layers, heads: int, head_dim: int, eps: float = 1e-6, ts_mid=None,
+                  quantized: bool = True):
+    """One DiT block's linears with attention between the first two, in the order of the page
+    "How fal made Ideogram V4 6x faster" (each large GEMM followed by its small op, fused).
+
+    ``layers``: four (W [K, N], bias [N] or None, gamma or None) for the QKV projection (gamma
+    over the Q and K columns), the output projection, the gated up-projection (W's columns are
+    gate | up halves) and the down-projection. hidden = heads * head_dim.
+
+    Steps; "bf16" is the rounding of a layer's output as it is stored between layers:
+      1. t = bf16(head_rmsnorm(x W_qkv + b_qkv)) over columns [0, 2 hidden) in heads of head_dim
+      2. q, k, v = t's three column blocks of width hidden; head h of each is its columns
+         [h head_dim, (h+1) head_dim)
+      3. a = bf16(attention(q, k, v)), heads side by side again
+      4. o = bf16(a W_o + b_o)
+      5. u = bf16(SiLU(o W_g + b_g) * (o W_u + b_u)); the NVFP4 scale handed to the next layer is
+         ``ts_mid`` if given, else amax(u) / 2688 (the static scale a calibration pass sets)
+      6. y = bf16(quant(u; ts_mid) W_down + b_down)
+    ``quantized`` False: every quantization and bf16 rounding dropped, the exact fp64 function
+    the quantized block approximates. Returns (y, dict of the intermediates and ts_mid).
+    """
+    hidden = heads * head_dim
+    rnd = round_to_bf16 if quantized else (lambda z: np.asarray(z, np.float64))
+    (w1, b1, g1), (w2, b2, _), (w3, b3, _), (w4, b4, _) = layers
+    M = x.shape[0]
+    t = rnd(_linear_ref(x, w1, b1, EPI_HEAD_RMSNORM, quantized, gamma=g1, head_dim=head_dim,
+                        norm_cols=2 * hidden, eps=eps))
+    qkv = t.reshape(M, 3, heads, head_dim).transpose(1, 2, 0, 3)    # [3, heads, M, head_dim]
+    a = rnd(attention_ref(qkv[0], qkv[1], qkv[2]).transpose(1, 0, 2).reshape(M, hidden))
+    o = rnd(_linear_ref(a, w2, b2, EPI_BIAS, quantized))
+    u = rnd(_linear_ref(o, w3, b3, EPI_GATED_SILU, quantized))
+    if quantized and ts_mid is None:
+        ts_mid = tensor_scale_ref(u)
+    y = rnd(_linear_ref(u, w4, b4, EPI_BIAS, quantized, tensor_scale=ts_mid))
+    return y, {"qkv": t, "attention": a, "out_proj": o, "up": u, "ts_mid": ts_mid}
