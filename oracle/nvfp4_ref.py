@@ -317,6 +317,12 @@ def gemm_ref(a_codes, a_scales, a_ts, b_codes, b_scales, b_ts, epilogue=EPI_BIAS
     """
     A = dequantize_ref(a_codes, a_scales, a_ts)
     B = dequantize_ref(b_codes, b_scales, b_ts)
+    return _gemm_epilogue_ref(A, B, epilogue, bias, gamma, head_dim, norm_cols, eps)
+
+
+def _gemm_epilogue_ref(A, B, epilogue, bias, gamma, head_dim, norm_cols, eps):
+    """epilogue(A @ B^T + bias) in fp64 for dequantized A [M, K] and B [N, K] (B's rows in
+    packed order for the gated epilogue, returned to original column order here)."""
     N = B.shape[0]
     if epilogue == EPI_GATED_SILU:
         B = B[np.argsort(gated_permutation(N))]  # packed rows back to original column order
@@ -371,6 +377,76 @@ def bf16_ulp(y: np.ndarray) -> np.ndarray:
     y = np.asarray(y, np.float64)
     _, e = np.frexp(np.where(y == 0, 1.0, y))
     return np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
+
+
+# ----------------------------------------------------------------------------------------
+# FP8 (E4M3) variant: per-tensor scaled operands, the same fused epilogues.
+#
+# Page "WaveSpeedAI x DataCrunch: FLUX real-time image inference on B200" (wavespeed.ai) lists
+# BF16/FP8 mixed precision through Blackwell's Transformer Engine among its optimizations;
+# page "FLUX.1-dev inference optimization with LoRAs" (aitime.ge) calls FP8 quantization lossy
+# but the best speed/memory trade-off. Neither fixes the scheme; read here as one fp32 scale
+# per tensor, ts = amax / 448 (E4M3's largest value), and per element
+# code = E4M3(fp32(x * fp32(1 / ts))), round to nearest even, saturating at 448, sign kept
+# (a negative value that rounds to zero is 0x80). A tensor with ts < 2**-126 (all zeros, or
+# so small that 1 / ts overflows) stores codes +0.
+# ----------------------------------------------------------------------------------------
+
+FP8_TENSOR_SCALE_DIVISOR = 448.0
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """fp32 -> signed E4M3 code: sign bit | E4M3 code of |v| (nearest even, saturating)."""
+    v = np.asarray(v, F32)
+    assert np.all(np.isfinite(v))
+    mag = np.minimum(np.abs(v), F32(2 * E4M3_MAX))  # anything above 448 saturates to 448
+    return (e4m3_encode_nonneg(mag) | (np.signbit(v).astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def fp8_tensor_scale_ref(x: np.ndarray) -> np.float32:
+    """ts = amax(|x|) / 448, one fp32 IEEE division."""
+    x = np.asarray(x, F32)
+    amax = F32(np.max(np.abs(x))) if x.size else F32(0.0)
+    return F32(amax / F32(FP8_TENSOR_SCALE_DIVISOR))
+
+
+def fp8_quantize_ref(x: np.ndarray, tensor_scale=None):
+    """x (fp32 array holding bf16 values) [M, K] -> (E4M3 codes [M, K] uint8, ts fp32).
+
+    ts = amax / 448 unless ``tensor_scale`` (a static scale) is given; inv = fp32(1 / ts);
+    code = E4M3(fp32(x * inv)).
+    """
+    x = np.asarray(x, F32)
+    assert np.all(np.isfinite(x)), "non-finite inputs are outside the format"
+    ts = fp8_tensor_scale_ref(x) if tensor_scale is None else F32(tensor_scale)
+    if not (ts >= FLT_MIN):
+        return np.zeros(x.shape, np.uint8), ts
+    inv = F32(F32(1.0) / ts)
+    with np.errstate(over="ignore"):
+        v = (x * inv).astype(F32)
+    return e4m3_encode(v), ts
+
+
+def fp8_pack_weights_ref(w: np.ndarray, gated_interleave: bool = False, tensor_scale=None):
+    """W [K, N] -> fp8_quantize_ref(W^T) with rows in packed order: (codes [N, K], ts)."""
+    wt = np.asarray(w, F32).T
+    if gated_interleave:
+        wt = wt[gated_permutation(wt.shape[0])]
+    return fp8_quantize_ref(np.ascontiguousarray(wt), tensor_scale)
+
+
+def fp8_dequantize_ref(codes: np.ndarray, ts) -> np.ndarray:
+    """x_hat = dec(code) * ts in fp64."""
+    return e4m3_decode(codes) * float(ts)
+
+
+def fp8_gemm_ref(a_codes, a_ts, b_codes, b_ts, epilogue=EPI_BIAS, bias=None, gamma=None,
+                 head_dim=256, norm_cols=0, eps=1e-6):
+    """y = epilogue(A_hat @ B_hat^T + bias) in fp64 for E4M3 A [M, K] and B [N, K] (K-major,
+    packed column order for the gated epilogue); the epilogues are those of gemm_ref."""
+    A = fp8_dequantize_ref(a_codes, a_ts)
+    B = fp8_dequantize_ref(b_codes, b_ts)
+    return _gemm_epilogue_ref(A, B, epilogue, bias, gamma, head_dim, norm_cols, eps)
 
 
 # ----------------------------------------------------------------------------------------
