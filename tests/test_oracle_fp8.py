@@ -23,7 +23,7 @@ def test_e4m3_every_finite_code_round_trips():
 @pytest.mark.parametrize("v,code", [
     (1.0, 0x38), (-1.0, 0xB8), (448.0, 0x7E), (-448.0, 0xFE),
     (449.0, 0x7E), (464.0, 0x7E),          # midpoint of 448 and (absent) 480: saturates
-    (1e30, 0x7E), (-1e30, 0xFE),
+    (1e30, 0x7E), (-1e30, 0xFE), (np.inf, 0x7E), (-np.inf, 0xFE),   # fp32 overflow saturates too
     (2.0 ** -9, 0x01),                     # smallest subnormal
     (2.0 ** -10, 0x00), (-(2.0 ** -10), 0x80),   # half of it: tie to the even code 0, sign kept
     (3 * 2.0 ** -11, 0x01),                # 0.75 of the smallest subnormal rounds up
