@@ -52,6 +52,10 @@ def parse_args(argv=None):
                    help="run one of the three layers only (for profiler captures)")
     p.add_argument("--chain", action="store_true",
                    help="up-projection -> down-projection at M=4608: fused NVFP4 output vs bf16 + quantize")
+    p.add_argument("--fp8", action="store_true",
+                   help="the three DiT GEMMs at M=4608 with FP8 (E4M3) operands: quantize + GEMM times")
+    p.add_argument("--spin-up-ms", type=float, default=300.0,
+                   help="--fp8: run the first GEMM this long before timing (clocks settle)")
     p.add_argument("--dit-block", action="store_true",
                    help="one DiT block's linears chained at 4608 tokens: per-stage CUDA-event times")
     p.add_argument("--sweep", action="store_true",
@@ -641,6 +645,66 @@ def run_chain(args):
                       "steps": args.steps}), flush=True)
 
 
+def run_fp8(args):
+    """The three DiT GEMMs at M=4608 in the FP8 variant (E4M3 operands, one scale per tensor, the
+    same fused epilogues): CUDA-event time of the activation quantize and of the GEMM, L2 flushed
+    before each timed call, against the FP8 dense peak (measured bf16 x 2); one JSON line per GEMM."""
+    import torch
+
+    import nvfp4_gemm_act_b300 as nv
+    from nvfp4_gemm_act_b300 import workloads as W
+    dev = "cuda:0"
+    peaks, _ = measured_peaks()
+    fp8_peak = peaks["bf16_tflops"] * 2.0
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    spun = False
+    for w in (W.QKV_RMSNORM, W.GATED_UP, W.DOWN_BIAS):
+        if args.only is not None and w.name != args.only:
+            continue
+        x = W.make_x(w).to(dev)
+        qb = nv.fp8_pack_weights(W.make_w(w).to(dev), gated_interleave=w.epilogue == "gated_silu")
+        b, g = W.make_bias(w), W.make_gamma(w)
+        bias = None if b is None else b.to(dev)
+        gamma = None if g is None else g.to(dev)
+        qa = nv._alloc_fp8(w.M, w.K, dev)
+        ws = torch.zeros(16, dtype=torch.uint8, device=dev)
+        out = torch.empty((w.M, w.out_cols), dtype=torch.bfloat16, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ops = {"quantize": lambda: nv.fp8_quantize(x, out=qa, workspace=ws),
+               "gemm": lambda: nv.fp8_gemm(qa, qb, w.epilogue, bias=bias, gamma=gamma, head_dim=w.head_dim,
+                                           norm_cols=w.norm_cols, eps=w.eps, out=out, device_error=err)}
+        if not spun and args.spin_up_ms > 0:  # keep the GPU busy until its clocks have settled
+            t0 = time.perf_counter()
+            while (time.perf_counter() - t0) * 1e3 < args.spin_up_ms:
+                for fn in ops.values():
+                    fn()
+                torch.cuda.synchronize()
+            spun = True
+        times = {"quantize": [], "gemm": []}
+        for it in range(max(args.warmup, 3)):
+            for fn in ops.values():
+                fn()
+        sampler = ClockSampler(0)
+        with sampler:
+            for it in range(args.steps):
+                for name, fn in ops.items():
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    fn()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    times[name].append(e0.elapsed_time(e1))
+        assert nv.nvfp4_get_device_error(err) == 0
+        qms, gms = float(np.median(times["quantize"])), float(np.median(times["gemm"]))
+        tf = w.flops / (gms / 1e3) / 1e12
+        print(json.dumps({"fp8": w.name, "M": w.M, "N": w.N, "K": w.K, "epilogue": w.epilogue,
+                          "gemm_ms": round(gms, 5), "gemm_tflops": round(tf, 1),
+                          "frac_of_measured_fp8": round(tf / fp8_peak, 4), "quantize_ms": round(qms, 5),
+                          "quantize_gbs": round(w.M * w.K * 3 / (qms / 1e3) / 1e9, 1),
+                          "clocks": sampler.summary()}), flush=True)
+
+
 def run_dit_block(args):
     """One DiT block at 4608 tokens (hidden 3072, 12 heads of 256, MLP 12288): the up-projection's
     static output scale calibrated once from its bf16 output, then per step (L2 flushed first)
@@ -697,6 +761,9 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.dit_block:
         run_dit_block(args)
+        return
+    if args.fp8:
+        run_fp8(args)
         return
     if args.chain:
         run_chain(args)

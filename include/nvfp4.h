@@ -208,6 +208,55 @@ NVFP4_API nvfp4_status nvfp4_gemm_nvfp4_out(const uint8_t *a_codes, const uint8_
                         float eps, const float *out_tensor_scale, uint8_t *out_codes,
                         uint8_t *out_scales, int *device_error, nvfp4_stream_t stream);
 
+/*
+ * FP8 variant -- E4M3 operands with one fp32 scale per tensor, the same fused GEMM and
+ * epilogues, for layers kept at higher precision than NVFP4. Pages "WaveSpeedAI x
+ * DataCrunch: FLUX real-time image inference on B200" (BF16/FP8 mixed precision through
+ * Blackwell's Transformer Engine) and "FLUX.1-dev inference optimization with LoRAs" (FP8
+ * quantization: lossy, the best speed/memory trade-off); neither fixes the scheme, which is:
+ *   ts = amax / 448 (448 = largest E4M3 value), fp32 IEEE division;
+ *   code = E4M3(fp32(x * fp32(1 / ts))), round to nearest even, saturating at +-448, sign
+ *   kept (a negative value that rounds to zero is 0x80);
+ *   a tensor with ts < 2^-126 (all zeros, or 1 / ts not finite) is stored as codes 0x00.
+ * Workspaces, streams, device errors and status codes are those of the NVFP4 calls.
+ */
+
+/*
+ * fp8_quantize -- x bf16 [M, K] (row stride ldx elements) -> codes uint8 [M, K] (contiguous,
+ * element k of row m at byte m * K + k), *tensor_scale = ts used (fp32, device).
+ *   tensor_scale_in  NULL: dynamic ts = amax(|x|) / 448 (two launches: amax, then encode;
+ *          `workspace` (nvfp4_workspace_bytes(), zero on first use) is left zeroed);
+ *          else a static fp32 ts on the device and `workspace` may be NULL.
+ * Rules: M >= 0 (M == 0 does nothing), K > 0, K % 64 == 0, ldx >= K, ldx % 8 == 0; x, codes,
+ * workspace 16-byte aligned, tensor_scale 4-byte aligned. Non-finite inputs: undefined.
+ */
+NVFP4_API nvfp4_status fp8_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, uint8_t *codes,
+                                    float *tensor_scale, const float *tensor_scale_in, void *workspace,
+                                    nvfp4_stream_t stream);
+
+/*
+ * fp8_pack_weights -- W bf16 [K, N] (row-major, x @ W) -> codes uint8 [N, K] (K-major: packed
+ * row p holds the K values of output column n(p)), *tensor_scale = amax(|W|) / 448.
+ *   gated_interleave  1: packed row 2j = column j (gate), 2j+1 = column N/2 + j (up), the
+ *          pairing of the gated-SiLU epilogue; 0: row p = column p.
+ * Rules: K % 64 == 0, N % 8 == 0, K / 64 <= 65535; w, codes, workspace 16-byte aligned.
+ */
+NVFP4_API nvfp4_status fp8_pack_weights(const void *w, int64_t K, int64_t N, int gated_interleave, uint8_t *codes,
+                                        float *tensor_scale, void *workspace, nvfp4_stream_t stream);
+
+/*
+ * fp8_gemm -- y = epilogue(a_ts * b_ts * (A B^T) + bias) with E4M3 A [M, K] and B [N, K] (codes
+ * from fp8_quantize and fp8_pack_weights), fp32 accumulation on the tensor cores
+ * (tcgen05.mma kind::f8f6f4); epilogue, bias, gamma, head_dim, norm_cols, eps, out_dtype,
+ * out, ldo, device_error and the rules are those of nvfp4_gemm (K % 64 == 0; a_codes, b_codes
+ * 16-byte aligned).
+ */
+NVFP4_API nvfp4_status fp8_gemm(const uint8_t *a_codes, const float *a_ts, const uint8_t *b_codes,
+                                const float *b_ts, int64_t M, int64_t N, int64_t K, nvfp4_epilogue epi,
+                                const float *bias, const float *gamma, int head_dim, int64_t norm_cols,
+                                float eps, nvfp4_out_dtype out_dtype, void *out, int64_t ldo,
+                                int *device_error, nvfp4_stream_t stream);
+
 /* Synchronizes `stream`, copies *device_error to *code, then zeroes the device word.
  * Returns NVFP4_ERR_NULL for NULL pointers, NVFP4_ERR_LAUNCH if a CUDA call fails. */
 NVFP4_API nvfp4_status nvfp4_get_device_error(int *device_error, int *code, nvfp4_stream_t stream);

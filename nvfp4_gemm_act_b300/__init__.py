@@ -43,6 +43,10 @@ _SIGS = {
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "fp8_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "fp8_pack_weights": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_int, _P, _P, _P, _P]),
+    "fp8_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P, ctypes.c_int, _I64,
+                                ctypes.c_float, ctypes.c_int, _P, _I64, _P, _P]),
 }
 
 
@@ -180,6 +184,68 @@ def nvfp4_gemm_nvfp4_out(a: Nvfp4Tensor, b: Nvfp4Tensor, epilogue: str, out_tens
         _ptr(a.codes), _ptr(a.scales), _ptr(a.ts), _ptr(b.codes), _ptr(b.scales), _ptr(b.ts),
         M, N, K, EPILOGUES[epilogue], _ptr(bias), _ptr(gamma), head_dim, norm_cols, eps,
         _ptr(out_tensor_scale), _ptr(out.codes), _ptr(out.scales), _ptr(device_error), _stream(stream)))
+    return out
+
+
+class Fp8Tensor(NamedTuple):
+    """A row-major FP8 (E4M3) matrix: codes uint8 [rows, K], fp32 tensor scale ts [1]."""
+    codes: torch.Tensor
+    ts: torch.Tensor
+    rows: int
+    K: int
+
+
+def _alloc_fp8(rows: int, K: int, device) -> Fp8Tensor:
+    return Fp8Tensor(torch.empty((rows, K), dtype=torch.uint8, device=device),
+                     torch.empty(1, dtype=torch.float32, device=device), rows, K)
+
+
+def fp8_quantize(x: torch.Tensor, tensor_scale_in: Optional[torch.Tensor] = None,
+                 out: Optional[Fp8Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                 stream=None) -> Fp8Tensor:
+    """bf16 [M, K] (row stride x.stride(0)) -> Fp8Tensor (one scale per tensor), via fp8_quantize."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if out is None:
+        out = _alloc_fp8(M, K, x.device)
+    if workspace is None and tensor_scale_in is None:
+        workspace = torch.zeros(nvfp4_workspace_bytes(), dtype=torch.uint8, device=x.device)
+    _check("fp8_quantize", lib().fp8_quantize(
+        _ptr(x), M, K, x.stride(0), _ptr(out.codes), _ptr(out.ts), _ptr(tensor_scale_in), _ptr(workspace),
+        _stream(stream)))
+    return out
+
+
+def fp8_pack_weights(w: torch.Tensor, gated_interleave: bool = False, out: Optional[Fp8Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> Fp8Tensor:
+    """bf16 W [K, N] -> K-major Fp8Tensor [N, K] (gated pair interleave optional)."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.is_contiguous()
+    K, N = w.shape
+    if out is None:
+        out = _alloc_fp8(N, K, w.device)
+    if workspace is None:
+        workspace = torch.zeros(nvfp4_workspace_bytes(), dtype=torch.uint8, device=w.device)
+    _check("fp8_pack_weights", lib().fp8_pack_weights(
+        _ptr(w), K, N, int(bool(gated_interleave)), _ptr(out.codes), _ptr(out.ts), _ptr(workspace),
+        _stream(stream)))
+    return out
+
+
+def fp8_gemm(a: Fp8Tensor, b: Fp8Tensor, epilogue: str = "bias", bias: Optional[torch.Tensor] = None,
+             gamma: Optional[torch.Tensor] = None, head_dim: int = 256, norm_cols: int = 0, eps: float = 1e-6,
+             out_dtype: torch.dtype = torch.bfloat16, out: Optional[torch.Tensor] = None,
+             device_error: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Fused FP8 GEMM: epilogue(a.ts * b.ts * A B^T + bias) -> out [M, N] (gated: [M, N/2])."""
+    assert a.K == b.K
+    M, N, K = a.rows, b.rows, a.K
+    width = N // 2 if epilogue == "gated_silu" else N
+    if out is None:
+        out = torch.empty((M, width), dtype=out_dtype, device=a.codes.device)
+    assert out.dtype == out_dtype and out.stride(1) == 1
+    _check("fp8_gemm", lib().fp8_gemm(
+        _ptr(a.codes), _ptr(a.ts), _ptr(b.codes), _ptr(b.ts), M, N, K, EPILOGUES[epilogue], _ptr(bias),
+        _ptr(gamma), head_dim, norm_cols, eps, OUT_DTYPES[out_dtype], _ptr(out), out.stride(0),
+        _ptr(device_error), _stream(stream)))
     return out
 
 

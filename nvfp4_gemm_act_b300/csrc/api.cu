@@ -185,14 +185,14 @@ nvfp4_status gemm_args(const uint8_t* a_codes, const uint8_t* a_scales, const fl
   return NVFP4_OK;
 }
 
-// Input pointer checks (after M == 0 has returned).
+// Input pointer checks (after M == 0 has returned); FP8 operands have no block scales.
 nvfp4_status gemm_inputs_ok(const nvfp4::GemmArgs& a) {
-  if (a.a_codes == nullptr || a.a_scales == nullptr || a.a_ts == nullptr || a.b_codes == nullptr ||
-      a.b_scales == nullptr || a.b_ts == nullptr)
+  if (a.a_codes == nullptr || a.a_ts == nullptr || a.b_codes == nullptr || a.b_ts == nullptr)
     return NVFP4_ERR_NULL;
+  if (!a.fp8 && (a.a_scales == nullptr || a.b_scales == nullptr)) return NVFP4_ERR_NULL;
   if (a.epi == NVFP4_EPI_HEAD_RMSNORM && a.gamma == nullptr && a.norm_cols > 0) return NVFP4_ERR_NULL;
-  if (!aligned16(a.a_codes) || !aligned16(a.a_scales) || !aligned16(a.b_codes) || !aligned16(a.b_scales))
-    return NVFP4_ERR_ALIGN;
+  if (!aligned16(a.a_codes) || !aligned16(a.b_codes)) return NVFP4_ERR_ALIGN;
+  if (!a.fp8 && (!aligned16(a.a_scales) || !aligned16(a.b_scales))) return NVFP4_ERR_ALIGN;
   return NVFP4_OK;
 }
 
@@ -247,6 +247,66 @@ nvfp4_status nvfp4_gemm_nvfp4_out(const uint8_t* a_codes, const uint8_t* a_scale
   a.out_codes = out_codes;
   a.out_scales = out_scales;
   a.out_ts = out_tensor_scale;
+  return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+nvfp4_status fp8_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes, float* tensor_scale,
+                          const float* tensor_scale_in, void* workspace, nvfp4_stream_t stream) {
+  if (M < 0 || K <= 0 || K % 64 != 0 || ldx < K) return NVFP4_ERR_SHAPE;
+  if (M > 0 && K > kMaxElems / M) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (x == nullptr || codes == nullptr || tensor_scale == nullptr) return NVFP4_ERR_NULL;
+  if (tensor_scale_in == nullptr && workspace == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(x) || ldx % 8 != 0 || !aligned16(codes) || (workspace != nullptr && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
+    return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  return from_cuda(nvfp4::launch_fp8_quantize(x, M, K, ldx, codes, static_cast<unsigned*>(workspace),
+                                              tensor_scale_in, tensor_scale, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+nvfp4_status fp8_pack_weights(const void* w, int64_t K, int64_t N, int gated_interleave, uint8_t* codes,
+                              float* tensor_scale, void* workspace, nvfp4_stream_t stream) {
+  if (w == nullptr || codes == nullptr || tensor_scale == nullptr || workspace == nullptr) return NVFP4_ERR_NULL;
+  if (gated_interleave != 0 && gated_interleave != 1) return NVFP4_ERR_ARG;
+  if (K <= 0 || K % 64 != 0 || N <= 0 || N % 8 != 0) return NVFP4_ERR_SHAPE;
+  if (K > kMaxElems / N || K / 64 > 65535) return NVFP4_ERR_SHAPE;
+  if (!aligned16(w) || !aligned16(codes) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
+    return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  unsigned* amax = static_cast<unsigned*>(workspace);
+  if (cudaMemsetAsync(amax, 0, nvfp4_workspace_bytes(), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  if (nvfp4_status st = from_cuda(nvfp4::launch_amax(w, K, N, N, amax, s)); st != NVFP4_OK) return st;
+  if (nvfp4_status st = from_cuda(nvfp4::launch_fp8_pack_weights(w, K, N, gated_interleave == 1, codes, amax,
+                                                                   tensor_scale, s));
+      st != NVFP4_OK)
+    return st;
+  return from_cuda(cudaMemsetAsync(amax, 0, nvfp4_workspace_bytes(), s));
+}
+
+nvfp4_status fp8_gemm(const uint8_t* a_codes, const float* a_ts, const uint8_t* b_codes, const float* b_ts, int64_t M,
+                      int64_t N, int64_t K, nvfp4_epilogue epi, const float* bias, const float* gamma, int head_dim,
+                      int64_t norm_cols, float eps, nvfp4_out_dtype out_dtype, void* out, int64_t ldo,
+                      int* device_error, nvfp4_stream_t stream) {
+  nvfp4::GemmArgs a;
+  int64_t out_cols = 0;
+  if (nvfp4_status st = gemm_args(a_codes, nullptr, a_ts, b_codes, nullptr, b_ts, M, N, K, epi, bias, gamma,
+                                  head_dim, norm_cols, eps, device_error, a, out_cols);
+      st != NVFP4_OK)
+    return st;
+  a.fp8 = 1;
+  if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32) return NVFP4_ERR_ARG;
+  if (ldo < out_cols) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (nvfp4_status st = gemm_inputs_ok(a); st != NVFP4_OK) return st;
+  if (out == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(out) || ldo % (out_dtype == NVFP4_OUT_BF16 ? 8 : 4) != 0) return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  a.out_fp32 = out_dtype == NVFP4_OUT_FP32 ? 1 : 0;
+  a.out = out;
+  a.ldo = ldo;
   return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -123,6 +123,13 @@ constexpr uint32_t make_idesc(int m, int n) {
 }
 constexpr uint32_t kIdesc = make_idesc(kCluster * kBM, kBN);
 
+// Instruction descriptor for kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B E4M3 (format 0 at
+// bits 7-9 and 10-12), both K-major, dense, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t make_idesc_f8(int m, int n) {
+  return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+constexpr uint32_t kIdescF8 = make_idesc_f8(kCluster * kBM, kBN);
+
 struct EpiParams {
   const float* a_ts;
   const float* b_ts;
@@ -297,11 +304,17 @@ __device__ __forceinline__ void epilogue_row(const EpiParams& p, const QuantOut&
   store_out<kHalf>(p, qo, tm_out, z, row0, c0, p.N, buf, lane);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                      const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
-                      const __grid_constant__ CUtensorMap tm_out, int K, int num_m_blocks, int num_tiles,
-                      EpiParams ep, int* err, uint64_t timeout_ns) {
+// The kernel for both operand formats. kFp8: E4M3 codes, K bytes a row, one scale per tensor
+// (kind::f8f6f4, K = 32 per MMA; a 128-byte stage row holds 128 K-elements); the scale
+// producer and the scale-copy warps have no work and the MMA thread waits on the full
+// barriers itself. Otherwise packed E2M1 codes with UE4M3 block scales (kind::mxf4nvf4,
+// K = 64 per MMA). A stage is 128 bytes of each row either way, so the ring, the shared
+// memory descriptors and the epilogue are the same.
+template <bool kFp8>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_sfa,
+                                          const CUtensorMap& tm_sfb, const CUtensorMap& tm_out, int K,
+                                          int num_m_blocks, int num_tiles, const EpiParams& ep, int* err,
+                                          uint64_t timeout_ns) {
   // num_tiles counts pair tiles: (row-tile pair, weight tile); row pairs fastest.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -321,8 +334,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_k_blocks = (K + kBK - 1) / kBK;
-  const int k_atoms = K / 64;                       // scale tiles per 128-row band
+  const int row_bytes = kFp8 ? K : K / 2;           // codes per row of A and of B
+  const int num_k_blocks = (row_bytes + kBKBytes - 1) / kBKBytes;
+  const int k_steps = row_bytes / 32;               // 32-byte MMA k-steps (K % 64 == 0)
+  const int k_atoms = K / 64;                       // NVFP4 scale tiles per 128-row band
   const int rank = static_cast<int>(cluster_ctarank());
   const bool leader = rank == 0;
   const int cluster_id = blockIdx.x / kCluster;
@@ -332,11 +347,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
-    prefetch_tmap(&tm_sfa);
-    prefetch_tmap(&tm_sfb);
+    if (!kFp8) {
+      prefetch_tmap(&tm_sfa);
+      prefetch_tmap(&tm_sfb);
+    }
     if (!ep.out_nvfp4) prefetch_tmap(&tm_out);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 2);            // the leader's two producers' arrivals (+ both CTAs' bytes)
+      mbar_init(full_bar(s), kFp8 ? 1 : 2);  // the leader's producers' arrivals (+ both CTAs' bytes)
       mbar_init(empty_bar(s), 1);           // the leader's MMA commit
       mbar_init(sf_bar(s), kSfWarps);       // one commit from each scale-copy warp
     }
@@ -422,22 +439,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int kb = 0; kb < num_k_blocks; ++kb) {
           const int s = kc % kStages;
-          // the scales are in both TMEMs: the scale warps commit sf_bar only after they saw
-          // the stage's full barrier, so the operands of both CTAs have landed too
-          if (!mbar_wait(sf_bar(s), (kc / kStages) & 1u, timeout_ns, err)) {
+          // NVFP4: the scales are in both TMEMs: the scale warps commit sf_bar only after they
+          // saw the stage's full barrier, so the operands of both CTAs have landed too.
+          // FP8: the operands of both CTAs have landed (the full barrier)
+          if (!mbar_wait(kFp8 ? full_bar(s) : sf_bar(s), (kc / kStages) & 1u, timeout_ns, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const int nk = min(kKStepsPerStage, k_atoms - kb * kKStepsPerStage);
+          const int nk = min(kKStepsPerStage, k_steps - kb * kKStepsPerStage);
           const uint32_t sf_col = tmem_base + kSfCol0 + s * kSfColsPerStage;
           const uint32_t a_s = sbase + kOffA + s * kABytes;
           const uint32_t b_s = sbase + kOffB + s * kBBytes;
           for (int j = 0; j < nk; ++j) {
             const uint64_t adesc = smem_desc(a_s + j * (kMmaK / 2), 16, 1024, kSwizzle128B);
             const uint64_t bdesc = smem_desc(b_s + j * (kMmaK / 2), 16, 1024, kSwizzle128B);
-            mma_nvf4_pair(tmem_base + kAccCol, adesc, bdesc, kIdesc, sf_col + j * 4,
-                          sf_col + kSfaColsPerStage + j * 8, (kb | j) != 0 ? 1u : 0u);
+            if constexpr (kFp8)
+              mma_f8_pair(tmem_base + kAccCol, adesc, bdesc, kIdescF8, (kb | j) != 0 ? 1u : 0u);
+            else
+              mma_nvf4_pair(tmem_base + kAccCol, adesc, bdesc, kIdesc, sf_col + j * 4,
+                            sf_col + kSfaColsPerStage + j * 8, (kb | j) != 0 ? 1u : 0u);
           }
           tc_commit_pair_mc(empty_bar(s), 0x3);  // release the stage in both CTAs
           ++kc;
@@ -450,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kSfWarp0 + kSfWarps) {
     warpgroup_reg_dealloc<kRegsLean>();
-    if (lane == 0 && leader) {
+    if (!kFp8 && lane == 0 && leader) {
       // ---------------- block-scale copies, shared -> TMEM (leader, for both CTAs) --------
       // scale warp w copies the scales of 64-deep k-step w of each stage: A, B band 0, B
       // band 1; the TMEM slot of stage s is free again once stage s has been refilled (the
@@ -487,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kEpiWarp0) {
     // warp 6: scale-tile producer; warp 7: no role (it fills warpgroup 1)
     warpgroup_reg_dealloc<kRegsLean>();
-    if (warp == kEpiWarp0 - 2 && lane == 0) producer(false);
+    if (!kFp8 && warp == kEpiWarp0 - 2 && lane == 0) producer(false);
   } else {
     // ---------------- epilogue warps (both CTAs) ----------------
     warpgroup_reg_alloc<kRegsEpilogue>();
@@ -584,6 +605,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                      const __grid_constant__ CUtensorMap tm_sfa, const __grid_constant__ CUtensorMap tm_sfb,
+                      const __grid_constant__ CUtensorMap tm_out, int K, int num_m_blocks, int num_tiles,
+                      const __grid_constant__ EpiParams ep, int* err, uint64_t timeout_ns) {
+  gemm_body<false>(tm_a, tm_b, tm_sfa, tm_sfb, tm_out, K, num_m_blocks, num_tiles, ep, err, timeout_ns);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_out, int K, int num_m_blocks, int num_tiles,
+                    const __grid_constant__ EpiParams ep, int* err, uint64_t timeout_ns) {
+  gemm_body<true>(tm_a, tm_b, tm_a, tm_a, tm_out, K, num_m_blocks, num_tiles, ep, err, timeout_ns);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -598,11 +634,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-bool encode_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+// Codes [rows, row_bytes] (K/2 bytes a row for NVFP4, K for FP8) in boxes of box_rows rows x
+// one 128-byte stage row, 128-byte swizzle.
+bool encode_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, uint32_t box_rows) {
   auto fn = get_encode_fn();
   if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBKBytes), box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -642,28 +680,52 @@ bool encode_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t width, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
+// Shared-memory opt-in and the register check, once per kernel: the setmaxnreg split assumes
+// the block is launched with 128 registers per thread (with fewer, the epilogue warpgroups'
+// increase could never be granted).
+template <typename Kernel>
+cudaError_t prepare_kernel(Kernel kernel) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
+  if (e == cudaSuccess && fa.numRegs != 128) e = cudaErrorInvalidConfiguration;
+  return e;
+}
+
+// As many clusters as can be resident at once (pairs are placed within a GPC).
+template <typename Kernel>
+int resident_clusters(Kernel kernel, const cudaLaunchConfig_t& cfg) {
+  int n = 0;
+  cudaLaunchConfig_t q = cfg;
+  q.gridDim = dim3(sm_count(), 1, 1);
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = sm_count() / kCluster;
+  }
+  return n;
+}
+
+}  // namespace
+
 nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   CUtensorMap tm_a, tm_b, tm_sfa, tm_sfb, tm_out;
-  if (!encode_codes_map(&tm_a, a.a_codes, a.M, a.K, kBM)) return NVFP4_ERR_LAUNCH;
-  if (!encode_codes_map(&tm_b, a.b_codes, a.N, a.K, kBRowsPerCta)) return NVFP4_ERR_LAUNCH;
-  if (!encode_scales_map(&tm_sfa, a.a_scales, a.M, a.K)) return NVFP4_ERR_LAUNCH;
-  if (!encode_scales_map(&tm_sfb, a.b_scales, a.N, a.K)) return NVFP4_ERR_LAUNCH;
+  const int64_t row_bytes = a.fp8 ? a.K : a.K / 2;
+  if (!encode_codes_map(&tm_a, a.a_codes, a.M, row_bytes, kBM)) return NVFP4_ERR_LAUNCH;
+  if (!encode_codes_map(&tm_b, a.b_codes, a.N, row_bytes, kBRowsPerCta)) return NVFP4_ERR_LAUNCH;
+  if (!a.fp8) {
+    if (!encode_scales_map(&tm_sfa, a.a_scales, a.M, a.K)) return NVFP4_ERR_LAUNCH;
+    if (!encode_scales_map(&tm_sfb, a.b_scales, a.N, a.K)) return NVFP4_ERR_LAUNCH;
+  }
   const int64_t width = a.epi == NVFP4_EPI_GATED_SILU ? a.N / 2 : a.N;
   if (a.out_nvfp4)
     std::memset(&tm_out, 0, sizeof(tm_out));  // unused: the NVFP4 output is stored directly
   else if (!encode_out_map(&tm_out, a.out, a.M, width, a.ldo, a.out_fp32 != 0))
     return NVFP4_ERR_LAUNCH;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    // the setmaxnreg split assumes the block is launched with 128 registers per thread: with
-    // fewer, the epilogue warpgroups' increase could never be granted
-    cudaFuncAttributes fa;
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, gemm_nvfp4_kernel);
-    if (attr_err == cudaSuccess && fa.numRegs != 128) attr_err = cudaErrorInvalidConfiguration;
-  });
-  if (attr_err != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  static const cudaError_t nvfp4_ready = prepare_kernel(gemm_nvfp4_kernel);
+  static const cudaError_t fp8_ready = prepare_kernel(gemm_fp8_kernel);
+  if ((a.fp8 ? fp8_ready : nvfp4_ready) != cudaSuccess) return NVFP4_ERR_LAUNCH;
   EpiParams ep;
   ep.a_ts = a.a_ts;
   ep.b_ts = a.b_ts;
@@ -696,22 +758,16 @@ nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // as many clusters as can be resident at once (pairs are placed within a GPC)
-  static int max_clusters = [&] {
-    int n = 0;
-    cudaLaunchConfig_t q = cfg;
-    q.gridDim = dim3(sm_count(), 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_kernel, &q) != cudaSuccess || n <= 0) {
-      (void)cudaGetLastError();
-      n = sm_count() / kCluster;
-    }
-    return n;
-  }();
-  const int clusters = std::max(1, std::min(num_pair_tiles, max_clusters));
+  static const int nvfp4_clusters = resident_clusters(gemm_nvfp4_kernel, cfg);
+  static const int fp8_clusters = resident_clusters(gemm_fp8_kernel, cfg);
+  const int clusters = std::max(1, std::min(num_pair_tiles, a.fp8 ? fp8_clusters : nvfp4_clusters));
   cfg.gridDim = dim3(clusters * kCluster, 1, 1);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, tm_a, tm_b, tm_sfa, tm_sfb, tm_out,
-                                           static_cast<int>(a.K), num_m, num_pair_tiles, ep, a.err,
-                                           wait_timeout_ns());
+  const int K = static_cast<int>(a.K);
+  const uint64_t limit = wait_timeout_ns();
+  const cudaError_t e =
+      a.fp8 ? cudaLaunchKernelEx(&cfg, gemm_fp8_kernel, tm_a, tm_b, tm_out, K, num_m, num_pair_tiles, ep, a.err, limit)
+            : cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, tm_a, tm_b, tm_sfa, tm_sfb, tm_out, K, num_m,
+                                 num_pair_tiles, ep, a.err, limit);
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH;
 }
 

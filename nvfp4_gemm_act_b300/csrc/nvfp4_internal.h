@@ -32,6 +32,15 @@ cudaError_t launch_pack_weights(const void* w, int64_t K, int64_t N, bool gated,
                                 uint8_t* codes, uint8_t* scales, const unsigned* amax_bits,
                                 float* ts_out, cudaStream_t s);
 
+// FP8 (E4M3, one scale per tensor): x [M, K] (row stride ldx) -> codes [M, K]; ts = *ts_in if
+// ts_in, else amax/448 of x (amax_kernel into ws[0], which the quantize kernel zeroes again).
+cudaError_t launch_fp8_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes, unsigned* ws,
+                               const float* ts_in, float* ts_out, cudaStream_t s);
+
+// W [K, N] -> E4M3 codes [N, K] (K-major, packed column order if gated), ts = amax/448.
+cudaError_t launch_fp8_pack_weights(const void* w, int64_t K, int64_t N, bool gated, uint8_t* codes,
+                                    const unsigned* amax_bits, float* ts_out, cudaStream_t s);
+
 struct GemmArgs {
   const uint8_t* a_codes;
   const uint8_t* a_scales;
@@ -55,6 +64,9 @@ struct GemmArgs {
   uint8_t* out_codes = nullptr;
   uint8_t* out_scales = nullptr;
   const float* out_ts = nullptr;
+  // operands: 0 = NVFP4 (codes [rows, K/2] + tiled block scales), 1 = FP8 E4M3 (codes
+  // [rows, K], no block scales; a_scales / b_scales unused)
+  int fp8 = 0;
 };
 
 // Validated arguments in, kernel launched (or an error code out).

@@ -425,6 +425,111 @@ __global__ void __launch_bounds__(256)
       static_cast<uint8_t>(bs.code);
 }
 
+// ---------------------------------------------------------------------------------------
+// FP8 (E4M3) with one scale per tensor: ts = amax / 448, code = E4M3(fp32(x * fp32(1 / ts))),
+// nearest even, saturating at +-448, sign kept; a tensor with ts < 2^-126 is stored as +0.
+// ---------------------------------------------------------------------------------------
+constexpr float kFp8TsDivisor = 448.0f;
+constexpr int kFp8Threads = 256;
+
+// 16 values -> 16 E4M3 codes, element i in byte i.
+__device__ __forceinline__ uint4 encode_e4m3x16(const float (&v)[16], float inv) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = cvt_e4m3x2(__fmul_rn(v[4 * i], inv), __fmul_rn(v[4 * i + 1], inv)) |
+           (cvt_e4m3x2(__fmul_rn(v[4 * i + 2], inv), __fmul_rn(v[4 * i + 3], inv)) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Activation quantizer: item = 16 consecutive elements of a row (32 bytes in, 16 bytes out),
+// grid-stride. Workspace words as for quantize_kernel: ws[0] = amax bits (from amax_kernel),
+// ws[1] = CTAs finished; the last CTA to finish zeroes both (dynamic scale only).
+__global__ void __launch_bounds__(kFp8Threads)
+    fp8_quantize_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M, uint32_t items_per_row,
+                        uint8_t* __restrict__ codes, unsigned* __restrict__ ws, const float* __restrict__ ts_in,
+                        float* __restrict__ ts_out) {
+  const float ts = ts_in != nullptr ? __ldg(ts_in)
+                                    : __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile unsigned*>(ws)),
+                                                kFp8TsDivisor);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *ts_out = ts;
+  const bool live = ts >= kFltMin;
+  const float inv = live ? __frcp_rn(ts) : 0.0f;
+  const uint64_t total = static_cast<uint64_t>(M) * items_per_row;
+  const uint64_t K = static_cast<uint64_t>(items_per_row) * 16u;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kFp8Threads + threadIdx.x; i < total;
+       i += static_cast<uint64_t>(gridDim.x) * kFp8Threads) {
+    const uint64_t r = i / items_per_row, c = (i - r * items_per_row) * 16u;
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (live) {
+      const __nv_bfloat16* src = x + r * ldx + c;
+      const uint4 lo = ld_nc_v4(src), hi = ld_nc_v4(src + 8);
+      const uint32_t wv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[2 * j] = bf16_lo(wv[j]);
+        v[2 * j + 1] = bf16_hi(wv[j]);
+      }
+      out = encode_e4m3x16(v, inv);
+    }
+    *reinterpret_cast<uint4*>(codes + r * K + c) = out;
+  }
+  if (ts_in == nullptr) {
+    __syncthreads();  // every thread of this CTA has read the amax word
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(ws + 1, 1u) == gridDim.x - 1u) {
+        ws[0] = 0u;
+        ws[1] = 0u;
+      }
+    }
+  }
+}
+
+// Weight packer: a CTA transposes a 64 (k) x 64 (n) tile of W through shared memory; each
+// thread then encodes 16 consecutive K-elements of one column into packed row p(n).
+template <bool kGated>
+__global__ void __launch_bounds__(256)
+    fp8_pack_weights_kernel(const __nv_bfloat16* __restrict__ w, uint32_t K, uint32_t N, uint8_t* __restrict__ codes,
+                            const unsigned* __restrict__ amax_bits, float* __restrict__ ts_out) {
+  __shared__ uint32_t tile[64][33];  // [k][n/2] bf16 pairs, padded against bank conflicts
+  const float ts = __fdiv_rn(__uint_as_float(*amax_bits), kFp8TsDivisor);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *ts_out = ts;
+  const bool live = ts >= kFltMin;
+  const float inv = live ? __frcp_rn(ts) : 0.0f;
+  const uint32_t n0 = blockIdx.x * 64u, k0 = blockIdx.y * 64u;
+  const uint32_t t = threadIdx.x;
+  {
+    const uint32_t kr = t >> 2, c = (t & 3u) * 16u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t n = n0 + c + h * 8u;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (n < N) v = ld_nc_v4(w + (uint64_t)(k0 + kr) * N + n);
+      uint32_t* dst = &tile[kr][(c + h * 8u) >> 1];
+      dst[0] = v.x;
+      dst[1] = v.y;
+      dst[2] = v.z;
+      dst[3] = v.w;
+    }
+  }
+  __syncthreads();
+  const uint32_t nl = t & 63u, b = t >> 6;  // column in tile, 16-row block in tile
+  const uint32_t n = n0 + nl;
+  if (n >= N) return;
+  float vals[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t word = tile[b * 16u + i][nl >> 1];
+    vals[i] = (nl & 1u) ? bf16_hi(word) : bf16_lo(word);
+  }
+  const uint4 out = live ? encode_e4m3x16(vals, inv) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t half = N >> 1;
+  const uint32_t p = kGated ? (n < half ? 2u * n : 2u * (n - half) + 1u) : n;
+  *reinterpret_cast<uint4*>(codes + (uint64_t)p * K + k0 + b * 16u) = out;
+}
+
 __global__ void wait_timeout_kernel(int* err, uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   if (threadIdx.x == 0) {
@@ -531,6 +636,34 @@ cudaError_t launch_pack_weights(const void* w, int64_t K, int64_t N, bool gated,
     pack_weights_kernel<false><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(w),
                                                     (uint32_t)K, (uint32_t)N, codes, scales,
                                                     amax_bits, ts_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes, unsigned* ws,
+                               const float* ts_in, float* ts_out, cudaStream_t s) {
+  if (ts_in == nullptr) {
+    const cudaError_t e = launch_amax(x, M, K, ldx, ws, s);
+    if (e != cudaSuccess) return e;
+  }
+  const uint32_t per_row = static_cast<uint32_t>(K / 16);
+  const uint64_t total = static_cast<uint64_t>(M) * per_row;
+  static const int per_sm = resident_blocks((const void*)fp8_quantize_kernel, kFp8Threads, 0);
+  const uint64_t want = (total + kFp8Threads - 1) / kFp8Threads;
+  const uint32_t grid = static_cast<uint32_t>(
+      std::max<uint64_t>(1u, std::min<uint64_t>(want, static_cast<uint64_t>(sm_count()) * per_sm)));
+  fp8_quantize_kernel<<<grid, kFp8Threads, 0, s>>>(static_cast<const __nv_bfloat16*>(x), static_cast<uint64_t>(ldx),
+                                                   static_cast<uint32_t>(M), per_row, codes, ws, ts_in, ts_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_pack_weights(const void* w, int64_t K, int64_t N, bool gated, uint8_t* codes,
+                                    const unsigned* amax_bits, float* ts_out, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((N + 63) / 64), static_cast<unsigned>(K / 64));
+  const __nv_bfloat16* wp = static_cast<const __nv_bfloat16*>(w);
+  if (gated)
+    fp8_pack_weights_kernel<true><<<grid, 256, 0, s>>>(wp, (uint32_t)K, (uint32_t)N, codes, amax_bits, ts_out);
+  else
+    fp8_pack_weights_kernel<false><<<grid, 256, 0, s>>>(wp, (uint32_t)K, (uint32_t)N, codes, amax_bits, ts_out);
   return cudaGetLastError();
 }
 

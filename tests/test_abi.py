@@ -153,8 +153,55 @@ def test_debug_timeout_host_checks():
     assert L.nvfp4_get_device_error(None, None, None) == ERR_NULL
 
 
+def f8g(**kw):
+    a = dict(ac=FAKE, ats=FAKE, bc=FAKE, bts=FAKE, M=128, N=256, K=256, epi=0, bias=None, gamma=None, hd=256,
+             nc=0, eps=1e-6, od=0, out=FAKE, ldo=256, err=None)
+    a.update(kw)
+    return nv.lib().fp8_gemm(a["ac"], a["ats"], a["bc"], a["bts"], a["M"], a["N"], a["K"], a["epi"], a["bias"],
+                             a["gamma"], a["hd"], a["nc"], a["eps"], a["od"], a["out"], a["ldo"], a["err"], None)
+
+
+def test_fp8_gemm_host_checks():
+    assert f8g(ac=None) == ERR_NULL
+    assert f8g(bts=None) == ERR_NULL
+    assert f8g(out=None) == ERR_NULL
+    assert f8g(epi=1, nc=256, gamma=None) == ERR_NULL
+    assert f8g(epi=5) == ERR_ARG
+    assert f8g(od=3) == ERR_ARG
+    assert f8g(K=96) == ERR_SHAPE
+    assert f8g(N=48, ldo=48) == ERR_SHAPE
+    assert f8g(ldo=128) == ERR_SHAPE
+    assert f8g(epi=2, ldo=128) != ERR_SHAPE
+    assert f8g(ac=FAKE + 1) == ERR_ALIGN
+    assert f8g(bc=FAKE + 8) == ERR_ALIGN
+    assert f8g(ldo=260) == ERR_ALIGN
+    assert f8g(M=0) == OK
+    assert f8g(M=0, ac=None, out=None) == OK
+
+
+def test_fp8_quantize_and_pack_host_checks():
+    L = nv.lib()
+    assert L.fp8_quantize(FAKE, 128, 96, 96, FAKE, FAKE, None, FAKE, None) == ERR_SHAPE    # K % 64
+    assert L.fp8_quantize(FAKE, 128, 128, 64, FAKE, FAKE, None, FAKE, None) == ERR_SHAPE   # ldx < K
+    assert L.fp8_quantize(FAKE, -1, 128, 128, FAKE, FAKE, None, FAKE, None) == ERR_SHAPE
+    assert L.fp8_quantize(FAKE, 0, 128, 128, None, None, None, None, None) == OK
+    assert L.fp8_quantize(None, 128, 128, 128, FAKE, FAKE, None, FAKE, None) == ERR_NULL
+    assert L.fp8_quantize(FAKE, 128, 128, 128, FAKE, FAKE, None, None, None) == ERR_NULL  # dynamic: workspace
+    assert L.fp8_quantize(FAKE, 128, 128, 132, FAKE, FAKE, None, FAKE, None) == ERR_ALIGN  # ldx % 8
+    assert L.fp8_quantize(FAKE, 128, 128, 128, FAKE + 8, FAKE, None, FAKE, None) == ERR_ALIGN
+    assert L.fp8_quantize(FAKE, 128, 128, 128, FAKE, FAKE + 2, None, FAKE, None) == ERR_ALIGN
+    assert L.fp8_pack_weights(None, 256, 256, 0, FAKE, FAKE, FAKE, None) == ERR_NULL
+    assert L.fp8_pack_weights(FAKE, 256, 256, 2, FAKE, FAKE, FAKE, None) == ERR_ARG
+    assert L.fp8_pack_weights(FAKE, 100, 256, 0, FAKE, FAKE, FAKE, None) == ERR_SHAPE
+    assert L.fp8_pack_weights(FAKE, 256, 12, 0, FAKE, FAKE, FAKE, None) == ERR_SHAPE
+    assert L.fp8_pack_weights(FAKE, 256, 256, 0, FAKE + 4, FAKE, FAKE, None) == ERR_ALIGN
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
 def test_valid_arguments_without_a_gpu_report_the_device():
     assert q() == ERR_DEVICE
     assert g() == ERR_DEVICE
+    assert f8g() == ERR_DEVICE
+    assert nv.lib().fp8_quantize(FAKE, 128, 128, 128, FAKE, FAKE, None, FAKE, None) == ERR_DEVICE
+    assert nv.lib().fp8_pack_weights(FAKE, 256, 256, 0, FAKE, FAKE, FAKE, None) == ERR_DEVICE
     assert nv.lib().nvfp4_debug_wait_timeout(FAKE, 1000, None) == ERR_DEVICE
