@@ -56,6 +56,10 @@ def parse_args(argv=None):
                    help="the three DiT GEMMs at M=4608 with FP8 (E4M3) operands: quantize + GEMM times")
     p.add_argument("--spin-up-ms", type=float, default=300.0,
                    help="--fp8: run the first GEMM this long before timing (clocks settle)")
+    p.add_argument("--attention", action="store_true",
+                   help="attention at 4608 tokens x 12 heads x 256: this package's kernel vs torch's")
+    p.add_argument("--attention-impl", choices=["kernel", "torch"], default="kernel",
+                   help="--dit-block: which attention the block uses")
     p.add_argument("--dit-block", action="store_true",
                    help="one DiT block's linears chained at 4608 tokens: per-stage CUDA-event times")
     p.add_argument("--sweep", action="store_true",
@@ -705,6 +709,76 @@ def run_fp8(args):
                           "clocks": sampler.summary()}), flush=True)
 
 
+def run_attention(args):
+    """Attention over a QKV projection output of 4608 tokens, 12 heads of 256 (Q, K, V ~ N(0,1)):
+    CUDA-event time of this package's kernel (V transpose + attention) and of torch's
+    scaled_dot_product_attention (its default choice, and the cuDNN backend where torch offers
+    it), L2 flushed before each call; 4 * M^2 * hidden FLOPs; one JSON line."""
+    import torch
+    import torch.nn.functional as F
+
+    import nvfp4_gemm_act_b300 as nv
+    from nvfp4_gemm_act_b300 import workloads as W
+    dev = "cuda:0"
+    M, heads, hd = 4608, 12, 256
+    H = heads * hd
+    qkv = W.attention_qkv(M, heads, seed=9).to(dev)
+    ws = torch.empty(nv.lib().attention_workspace_bytes(M, heads), dtype=torch.uint8, device=dev)
+    out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    q, k, v = qkv.view(M, 3, heads, hd).permute(1, 2, 0, 3).unsqueeze(1).unbind(0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    impls = {"kernel": lambda: nv.attention(qkv, heads, out=out, workspace=ws, device_error=err),
+             "torch_default": lambda: F.scaled_dot_product_attention(q, k, v)}
+    try:
+        from torch.nn.attention import SDPBackend, sdpa_kernel
+
+        def cudnn():
+            with sdpa_kernel([SDPBackend.CUDNN_ATTENTION]):
+                return F.scaled_dot_product_attention(q, k, v)
+        cudnn()
+        torch.cuda.synchronize()
+        impls["torch_cudnn"] = cudnn
+    except Exception as e:  # not offered for this shape / build
+        print(json.dumps({"note": f"cudnn backend unavailable: {type(e).__name__}"}), flush=True)
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < 0.3:  # clocks settle
+        impls["kernel"]()
+        torch.cuda.synchronize()
+    res = {}
+    sampler = ClockSampler(0)
+    for name, fn in impls.items():
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        ts = []
+        with sampler if name == "kernel" else _nullctx():
+            for _ in range(args.steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+        res[name] = float(np.median(ts))
+    assert nv.nvfp4_get_device_error(err) == 0
+    flops = 4 * M * M * H
+    peaks, _ = measured_peaks()
+    print(json.dumps({"attention": f"M={M} heads={heads}x{hd}, no mask, bf16",
+                      "ms": {k: round(v, 5) for k, v in res.items()},
+                      "tflops": {k: round(flops / (v / 1e3) / 1e12, 1) for k, v in res.items()},
+                      "kernel_frac_of_measured_bf16": round(flops / (res["kernel"] / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                      "steps": args.steps, "clocks": sampler.summary()}), flush=True)
+
+
+class _nullctx:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
 def run_dit_block(args):
     """One DiT block at 4608 tokens (hidden 3072, 12 heads of 256, MLP 12288): the up-projection's
     static output scale calibrated once from its bf16 output, then per step (L2 flushed first)
@@ -715,7 +789,7 @@ def run_dit_block(args):
     from nvfp4_gemm_act_b300.dit_block import STAGES, seeded_dit_block
     dev = "cuda:0"
     M = 4608
-    blk, x = seeded_dit_block(M, dev)
+    blk, x = seeded_dit_block(M, dev, attention_impl=args.attention_impl)
     blk.calibrate(x)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     times = {}
@@ -751,7 +825,8 @@ def run_dit_block(args):
                       "share": {k: round(v / sum(ms.values()), 4) for k, v in ms.items()},
                       "tflops": {k: round(flops[k] / (ms[k] / 1e3) / 1e12, 1) for k in STAGES},
                       "nvfp4_gemm_tflops_block": round(blk.gemm_flops(M) / ((tot - ms["attention"]) / 1e3) / 1e12, 1),
-                      "attention": "torch scaled_dot_product_attention, bf16",
+                      "attention": ("this package's attention kernel" if args.attention_impl == "kernel"
+                                    else "torch scaled_dot_product_attention") + ", bf16",
                       "steps": args.steps, "l2": "flushed before each block",
                       "clocks": sampler.summary()}), flush=True)
 
@@ -764,6 +839,9 @@ def main(argv=None):
         return
     if args.fp8:
         run_fp8(args)
+        return
+    if args.attention:
+        run_attention(args)
         return
     if args.chain:
         run_chain(args)

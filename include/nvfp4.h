@@ -257,6 +257,35 @@ NVFP4_API nvfp4_status fp8_gemm(const uint8_t *a_codes, const float *a_ts, const
                                 float eps, nvfp4_out_dtype out_dtype, void *out, int64_t ldo,
                                 int *device_error, nvfp4_stream_t stream);
 
+/*
+ * Attention -- the DiT block's other large op, between the QKV projection and the output
+ * projection (page "How fal made Ideogram V4 6x faster": a pass costs the sum of its layers).
+ * Scaled dot-product attention per head, no mask, bf16 in and out, fp32 softmax and
+ * accumulation on the tensor cores (tcgen05.mma kind::f16):
+ *   out[m, h*D + d] = sum_j softmax_j(q_m . k_j / sqrt(D)) v_j[d],   D = head_dim = 256,
+ * with q_m = qkv[m, h*D .. h*D + D), k_j = qkv[j, H + h*D ..), v_j = qkv[j, 2H + h*D ..),
+ * H = heads * D: the layout the QKV GEMM writes (Q | K | V, heads side by side in each).
+ * The probabilities are rounded to bf16 before they multiply V (as FlashAttention kernels
+ * do), so results match exact attention to about 2^-9 relative, not bit for bit.
+ */
+
+/* Bytes of the attention_fwd workspace (V transposed, bf16 [heads * 256, round_up(M, 8)]);
+ * 0 for M <= 0 or heads <= 0. */
+NVFP4_API size_t attention_workspace_bytes(int64_t M, int heads);
+
+/*
+ * attention_fwd -- qkv bf16 [M, ld_qkv >= 3 * heads * 256] -> out bf16 [M, ldo >= heads * 256].
+ * workspace: attention_workspace_bytes(M, heads) bytes of device memory (contents need not
+ * be initialised; overwritten). Two launches on `stream`: the V transpose, then the attention
+ * kernel (one CTA per 128 queries and head).
+ * Rules: head_dim == 256 (else NVFP4_ERR_ARG); 1 <= heads <= 256; M >= 0 (M == 0 does
+ * nothing); ld_qkv and ldo multiples of 8; qkv, workspace, out 16-byte aligned.
+ * device_error: as for nvfp4_gemm (a bounded wait that expired writes NVFP4_ERR_TIMEOUT).
+ */
+NVFP4_API nvfp4_status attention_fwd(const void *qkv, int64_t M, int64_t ld_qkv, int heads, int head_dim,
+                                     void *workspace, void *out, int64_t ldo, int *device_error,
+                                     nvfp4_stream_t stream);
+
 /* Synchronizes `stream`, copies *device_error to *code, then zeroes the device word.
  * Returns NVFP4_ERR_NULL for NULL pointers, NVFP4_ERR_LAUNCH if a CUDA call fails. */
 NVFP4_API nvfp4_status nvfp4_get_device_error(int *device_error, int *code, nvfp4_stream_t stream);

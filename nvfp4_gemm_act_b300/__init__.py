@@ -47,6 +47,8 @@ _SIGS = {
     "fp8_pack_weights": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_int, _P, _P, _P, _P]),
     "fp8_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P, ctypes.c_int, _I64,
                                 ctypes.c_float, ctypes.c_int, _P, _I64, _P, _P]),
+    "attention_workspace_bytes": (ctypes.c_size_t, [_I64, ctypes.c_int]),
+    "attention_fwd": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_int, ctypes.c_int, _P, _P, _I64, _P, _P]),
 }
 
 
@@ -245,6 +247,25 @@ def fp8_gemm(a: Fp8Tensor, b: Fp8Tensor, epilogue: str = "bias", bias: Optional[
     _check("fp8_gemm", lib().fp8_gemm(
         _ptr(a.codes), _ptr(a.ts), _ptr(b.codes), _ptr(b.ts), M, N, K, EPILOGUES[epilogue], _ptr(bias),
         _ptr(gamma), head_dim, norm_cols, eps, OUT_DTYPES[out_dtype], _ptr(out), out.stride(0),
+        _ptr(device_error), _stream(stream)))
+    return out
+
+
+def attention(qkv: torch.Tensor, heads: int, head_dim: int = 256, out: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None, device_error: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    """Scaled dot-product attention over the QKV projection's output qkv bf16 [M, >= 3 H]
+    (Q | K | V, heads of head_dim side by side; H = heads * head_dim) -> bf16 [M, H]."""
+    assert qkv.dtype == torch.bfloat16 and qkv.dim() == 2 and qkv.stride(1) == 1
+    M = qkv.shape[0]
+    H = heads * head_dim
+    if out is None:
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=qkv.device)
+    if workspace is None:
+        workspace = torch.empty(max(lib().attention_workspace_bytes(M, heads), 16), dtype=torch.uint8,
+                                device=qkv.device)
+    _check("attention_fwd", lib().attention_fwd(
+        _ptr(qkv), M, qkv.stride(0), heads, head_dim, _ptr(workspace), _ptr(out), out.stride(0),
         _ptr(device_error), _stream(stream)))
     return out
 

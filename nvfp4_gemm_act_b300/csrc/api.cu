@@ -310,6 +310,26 @@ nvfp4_status fp8_gemm(const uint8_t* a_codes, const float* a_ts, const uint8_t* 
   return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t attention_workspace_bytes(int64_t M, int heads) {
+  if (M <= 0 || heads <= 0) return 0;
+  return static_cast<size_t>(heads) * 256u * static_cast<size_t>(nvfp4::attention_vt_ld(M)) * 2u;
+}
+
+nvfp4_status attention_fwd(const void* qkv, int64_t M, int64_t ld_qkv, int heads, int head_dim, void* workspace,
+                           void* out, int64_t ldo, int* device_error, nvfp4_stream_t stream) {
+  if (head_dim != 256) return NVFP4_ERR_ARG;
+  if (heads <= 0 || heads > 256 || M < 0 || M > (int64_t(1) << 31) - 1) return NVFP4_ERR_SHAPE;
+  const int64_t hidden = static_cast<int64_t>(heads) * head_dim;
+  if (ld_qkv < 3 * hidden || ldo < hidden) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;
+  if (qkv == nullptr || workspace == nullptr || out == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(qkv) || !aligned16(workspace) || !aligned16(out) || ld_qkv % 8 != 0 || ldo % 8 != 0)
+    return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  return nvfp4::launch_attention(qkv, M, ld_qkv, heads, workspace, out, ldo, device_error,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
 nvfp4_status nvfp4_get_device_error(int* device_error, int* code, nvfp4_stream_t stream) {
   if (device_error == nullptr || code == nullptr) return NVFP4_ERR_NULL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -72,6 +72,14 @@ struct GemmArgs {
 // Validated arguments in, kernel launched (or an error code out).
 nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s);
 
+// Row stride (elements) of the V^T workspace [heads * 256, attention_vt_ld(M)] bf16.
+int64_t attention_vt_ld(int64_t M);
+
+// Attention over qkv [M, 3 * heads * 256] (Q | K | V, heads contiguous in each, row stride
+// ld_qkv) -> out [M, heads * 256] (row stride ldo): V^T into `vt`, then the attention kernel.
+nvfp4_status launch_attention(const void* qkv, int64_t M, int64_t ld_qkv, int heads, void* vt, void* out,
+                              int64_t ldo, int* err, cudaStream_t s);
+
 cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace nvfp4

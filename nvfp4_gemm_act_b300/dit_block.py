@@ -22,6 +22,7 @@ from typing import Dict, List, Optional
 import torch
 import torch.nn.functional as F
 
+from . import attention as attention_fwd
 from . import nvfp4_gemm, nvfp4_gemm_nvfp4_out, nvfp4_pack_weights, nvfp4_quantize
 from . import workloads as W
 
@@ -36,7 +37,9 @@ class DitBlockLinears:
     """
 
     def __init__(self, w_qkv, b_qkv, gamma, w_o, b_o, w_up, b_up, w_down, b_down, heads: int,
-                 head_dim: int = 256, eps: float = 1e-6, device="cuda:0"):
+                 head_dim: int = 256, eps: float = 1e-6, device="cuda:0", attention_impl: str = "torch"):
+        assert attention_impl in ("kernel", "torch")
+        self.attention_impl = attention_impl
         self.heads, self.head_dim, self.eps = heads, head_dim, eps
         self.hidden = heads * head_dim
         self.mlp = w_up.shape[1] // 2
@@ -62,7 +65,13 @@ class DitBlockLinears:
                           gamma=self.gamma, head_dim=self.head_dim, norm_cols=2 * self.hidden, eps=self.eps)
 
     def attention(self, t):
-        """t [M, 3 hidden] (Q | K | V, heads side by side in each) -> [M, hidden]."""
+        """t [M, 3 hidden] (Q | K | V, heads side by side in each) -> [M, hidden]: this
+        package's attention kernel, or torch's scaled_dot_product_attention."""
+        if self.attention_impl == "kernel":
+            return attention_fwd(t, self.heads, self.head_dim)
+        return self.attention_torch(t)
+
+    def attention_torch(self, t):
         M = t.shape[0]
         q, k, v = t.view(M, 3, self.heads, self.head_dim).permute(1, 2, 0, 3).unsqueeze(1).unbind(0)
         a = F.scaled_dot_product_attention(q, k, v)                  # [1, heads, M, head_dim]
@@ -125,11 +134,12 @@ class DitBlockLinears:
 
 
 def seeded_dit_block(M: int = 4608, device="cuda:0", seed: Optional[int] = None,
-                     heads: int = W.DIT_HEADS, mlp: int = 12288):
+                     heads: int = W.DIT_HEADS, mlp: int = 12288, attention_impl: str = "torch"):
     """The seeded synthetic block (random-initialised weights of the four layers, drawn by
     ``workloads.dit_block``) on ``device``, and its bf16 input [M, heads * 256]."""
     qkv, o, up, down = W.dit_block(M, seed, heads=heads, mlp=mlp)
     blk = DitBlockLinears(W.make_w(qkv), W.make_bias(qkv), W.make_gamma(qkv), W.make_w(o), W.make_bias(o),
                           W.make_w(up), W.make_bias(up), W.make_w(down), W.make_bias(down),
-                          heads=heads, head_dim=qkv.head_dim, eps=qkv.eps, device=device)
+                          heads=heads, head_dim=qkv.head_dim, eps=qkv.eps, device=device,
+                          attention_impl=attention_impl)
     return blk, W.make_x(qkv).to(device)

@@ -158,3 +158,12 @@ def make_gamma(w: Workload) -> Optional[torch.Tensor]:
         return None
     g = 1.0 + w.gamma_std * _rng(w.layer_seed, 3).standard_normal(w.norm_cols)
     return torch.from_numpy(g.astype(np.float32))
+
+
+def attention_qkv(M: int, heads: int, seed: int, q_scale: float = 1.0, head_dim: int = 256) -> torch.Tensor:
+    """A QKV projection output [M, 3 * heads * head_dim] as a CPU bf16 tensor: Q, K, V ~ N(0, 1),
+    Q times ``q_scale`` (larger logits), drawn from ``default_rng((seed, 5))``."""
+    x = _rng(seed, 5).standard_normal((M, 3 * heads * head_dim))
+    x[:, : heads * head_dim] *= q_scale
+    return _bf16(x)
+

@@ -197,11 +197,35 @@ def test_fp8_quantize_and_pack_host_checks():
     assert L.fp8_pack_weights(FAKE, 256, 256, 0, FAKE + 4, FAKE, FAKE, None) == ERR_ALIGN
 
 
+def test_attention_host_checks():
+    L = nv.lib()
+
+    def a(**kw):
+        d = dict(qkv=FAKE, M=256, ld=3 * 512, heads=2, hd=256, ws=FAKE, out=FAKE, ldo=512)
+        d.update(kw)
+        return L.attention_fwd(d["qkv"], d["M"], d["ld"], d["heads"], d["hd"], d["ws"], d["out"], d["ldo"], None,
+                               None)
+    assert a(hd=128) == ERR_ARG
+    assert a(heads=0) == ERR_SHAPE
+    assert a(ld=1000) == ERR_SHAPE          # < 3 * heads * 256
+    assert a(ldo=256) == ERR_SHAPE
+    assert a(M=-1) == ERR_SHAPE
+    assert a(M=0, qkv=None, ws=None, out=None) == OK
+    assert a(qkv=None) == ERR_NULL
+    assert a(ws=None) == ERR_NULL
+    assert a(out=None) == ERR_NULL
+    assert a(qkv=FAKE + 2) == ERR_ALIGN
+    assert a(ld=1540) == ERR_ALIGN
+    assert L.attention_workspace_bytes(100, 2) == 2 * 256 * 104 * 2
+    assert L.attention_workspace_bytes(0, 2) == 0
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
 def test_valid_arguments_without_a_gpu_report_the_device():
     assert q() == ERR_DEVICE
     assert g() == ERR_DEVICE
     assert f8g() == ERR_DEVICE
+    assert nv.lib().attention_fwd(FAKE, 256, 1536, 2, 256, FAKE, FAKE, 512, None, None) == ERR_DEVICE
     assert nv.lib().fp8_quantize(FAKE, 128, 128, 128, FAKE, FAKE, None, FAKE, None) == ERR_DEVICE
     assert nv.lib().fp8_pack_weights(FAKE, 256, 256, 0, FAKE, FAKE, FAKE, None) == ERR_DEVICE
     assert nv.lib().nvfp4_debug_wait_timeout(FAKE, 1000, None) == ERR_DEVICE
