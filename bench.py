@@ -55,7 +55,7 @@ def parse_args(argv=None):
     p.add_argument("--fp8", action="store_true",
                    help="the three DiT GEMMs at M=4608 with FP8 (E4M3) operands: quantize + GEMM times")
     p.add_argument("--spin-up-ms", type=float, default=300.0,
-                   help="--fp8: run the first GEMM this long before timing (clocks settle)")
+                   help="--fp8, --attention: keep the GPU busy this long before timing (clocks settle)")
     p.add_argument("--attention", action="store_true",
                    help="attention at 4608 tokens x 12 heads x 256: this package's kernel vs torch's")
     p.add_argument("--attention-impl", choices=["kernel", "torch"], default="kernel",
@@ -742,7 +742,7 @@ def run_attention(args):
     except Exception as e:  # not offered for this shape / build
         print(json.dumps({"note": f"cudnn backend unavailable: {type(e).__name__}"}), flush=True)
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < 0.3:  # clocks settle
+    while (time.perf_counter() - t0) * 1e3 < args.spin_up_ms:  # clocks settle
         impls["kernel"]()
         torch.cuda.synchronize()
     res = {}

@@ -8,9 +8,12 @@
 //   out[m, h*256 + d] = sum_j softmax_j(q_m . k_j / 16) v_j[d]      (per head h)
 //
 // Design: one CTA per (128-query tile, head), one CTA per SM (224 KB of shared memory).
-//   warp 0     TMA producer: the Q tile once (4 boxes of 128 rows x 64 columns), then per
-//              64-key tile the K tile (4 boxes of 64 x 64) and the V^T tile (256 x 64) into a
-//              2-stage ring;
+//   warp 0     TMA producer of Q (once: 4 boxes of 128 rows x 64 columns) and of the K tiles
+//              (4 boxes of 64 keys x 64) into a 2-stage ring; a K stage is free again as soon
+//              as the S MMAs that read it have completed;
+//   warp 2     TMA producer of the V^T tiles (256 x 64 keys) into their own 2-stage ring; a V
+//              stage is free again when the PV MMAs that read it have completed. With the two
+//              rings released separately, K tiles are fetched about two tiles ahead of use;
 //   warp 1     TMEM allocation (512 columns: two 64-column S buffers, a 256-column O) and the
 //              MMA-issuing thread: S_j = Q K_j^T (M128 N64, 16 x K16), then O += P_{j-1} V_{j-1}
 //              (M128 N256, 4 x K16), so that the softmax of tile j runs while PV_{j-1} does;
@@ -40,14 +43,14 @@ namespace {
 constexpr int kHd = 256;            // head_dim
 constexpr int kBQ = 128;            // queries per CTA (TMEM lanes)
 constexpr int kBKV = 64;            // keys per tile
-constexpr int kStages = 2;          // K / V^T ring
+constexpr int kStages = 2;          // K ring and V^T ring
 constexpr int kChunk = 64;          // bf16 elements in one 128-byte swizzle row
 constexpr int kQChunkBytes = kBQ * 128;        // 16 KB
 constexpr int kQBytes = (kHd / kChunk) * kQChunkBytes;   // 64 KB
 constexpr int kKChunkBytes = kBKV * 128;       // 8 KB
 constexpr int kKBytes = (kHd / kChunk) * kKChunkBytes;   // 32 KB
 constexpr int kVBytes = kHd * 128;             // 32 KB: 256 rows (d) x 64 keys
-constexpr int kStageBytes = kKBytes + kVBytes;
+constexpr int kStageBytes = kKBytes + kVBytes;   // K stage b, then V^T stage b
 constexpr int kPBytes = kBQ * 128;             // 16 KB: 128 rows x 64 keys
 constexpr int kOffQ = 0;
 constexpr int kOffKV = kOffQ + kQBytes;
@@ -97,6 +100,13 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr) { return smem_desc(addr, 16, 1024, kSwizzle128B); }
 
+// 2^x with the MUFU approximation (ex2.approx.ftz.f32: about 2 ulp; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_vt, int M, int hidden, __nv_bfloat16* __restrict__ out,
@@ -105,17 +115,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  // bars: [0] Q full; [1, 3) K/V stage full; [3, 5) S buffer full (MMA commit); [5, 7) S
-  // buffer read (4 softmax warps); [7, 9) P buffer written (4 softmax warps); [9, 11) PV
-  // done with P buffer b (MMA commit: P buffer and K/V stage free, O updated); [11] drain
+  // bars: [0] Q full; [1, 3) K stage full; [3, 5) S buffer full (MMA commit: S_j in TMEM,
+  // K stage free); [5, 7) S buffer read (4 softmax warps); [7, 9) P buffer written (4
+  // softmax warps); [9, 11) PV done with P buffer b (MMA commit: P buffer and V stage free,
+  // O updated); [11] drain; [12, 14) V stage full
   const uint32_t q_full = smem_u32(bars);
-  auto kv_full = [&](int b) { return smem_u32(bars + 1 + b); };
+  auto k_full = [&](int b) { return smem_u32(bars + 1 + b); };
   auto s_full = [&](int b) { return smem_u32(bars + 3 + b); };
   auto s_free = [&](int b) { return smem_u32(bars + 5 + b); };
   auto p_full = [&](int b) { return smem_u32(bars + 7 + b); };
   auto pv_done = [&](int b) { return smem_u32(bars + 9 + b); };
   const uint32_t drain_bar = smem_u32(bars + 11);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  auto v_full = [&](int b) { return smem_u32(bars + 12 + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -129,7 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_vt);
     mbar_init(q_full, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(kv_full(b), 1);
+      mbar_init(k_full(b), 1);
+      mbar_init(v_full(b), 1);
       mbar_init(s_full(b), 1);
       mbar_init(s_free(b), 4);
       mbar_init(p_full(b), 4);
@@ -147,30 +160,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producers: Q and K (warp 0), V^T (warp 2) ----------------
+      const bool kpart = warp == 0;
       const uint64_t pol = policy_evict_normal();
-      const int qcol = head * kHd, kcol = hidden + head * kHd;
-      mbar_arrive_expect_tx(q_full, kQBytes);
-      for (int c = 0; c < kHd / kChunk; ++c)
-        tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, qcol + c * kChunk, q0, q_full, pol);
+      if (kpart) {
+        mbar_arrive_expect_tx(q_full, kQBytes);
+        for (int c = 0; c < kHd / kChunk; ++c)
+          tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, head * kHd + c * kChunk, q0, q_full, pol);
+      }
+      const int kcol = hidden + head * kHd;
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int b = j & 1;
-        if (j >= 2 && !mbar_wait(pv_done(b), ((j - 2) >> 1) & 1u, timeout_ns, err)) break;
+        // the stage's previous tile (j - 2) has been read: by S_{j-2} (K) or PV_{j-2} (V)
+        if (j >= 2 && !mbar_wait(kpart ? s_full(b) : pv_done(b), ((j - 2) >> 1) & 1u, timeout_ns, err)) break;
         const uint32_t stage = sbase + kOffKV + b * kStageBytes;
-        mbar_arrive_expect_tx(kv_full(b), kStageBytes);
-        for (int c = 0; c < kHd / kChunk; ++c)
-          tma_load_2d(stage + c * kKChunkBytes, &tm_k, kcol + c * kChunk, j * kBKV, kv_full(b), pol);
-        tma_load_2d(stage + kKBytes, &tm_vt, j * kBKV, head * kHd, kv_full(b), pol);
+        if (kpart) {
+          mbar_arrive_expect_tx(k_full(b), kKBytes);
+          for (int c = 0; c < kHd / kChunk; ++c)
+            tma_load_2d(stage + c * kKChunkBytes, &tm_k, kcol + c * kChunk, j * kBKV, k_full(b), pol);
+        } else {
+          mbar_arrive_expect_tx(v_full(b), kVBytes);
+          tma_load_2d(stage + kKBytes, &tm_vt, j * kBKV, head * kHd, v_full(b), pol);
+        }
         issued = j + 1;
       }
       // No copy may still be in flight when the CTA exits: the last two stages' loads (the
       // earlier ones were waited for before their stage was reused) and the Q tile.
-      (void)mbar_wait(q_full, 0u, timeout_ns, err);
+      if (kpart) (void)mbar_wait(q_full, 0u, timeout_ns, err);
       for (int j = issued >= 2 ? issued - 2 : 0; j < issued; ++j)
-        (void)mbar_wait(kv_full(j & 1), (j >> 1) & 1u, timeout_ns, err);
+        (void)mbar_wait(kpart ? k_full(j & 1) : v_full(j & 1), (j >> 1) & 1u, timeout_ns, err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -178,7 +199,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(q_full, 0u, timeout_ns, err);
       auto issue_pv = [&](int i) {
         const int b = i & 1;
-        if (!mbar_wait(p_full(b), (i >> 1) & 1u, timeout_ns, err)) return false;
+        if (!mbar_wait(v_full(b), (i >> 1) & 1u, timeout_ns, err) ||
+            !mbar_wait(p_full(b), (i >> 1) & 1u, timeout_ns, err))
+          return false;
         tc_fence_after();
         const uint32_t p_s = sbase + kOffP + b * kPBytes;
         const uint32_t v_s = sbase + kOffKV + b * kStageBytes + kKBytes;
@@ -191,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int j = 0; j < nt && ok; ++j) {
         const int b = j & 1;
-        ok = mbar_wait(kv_full(b), (j >> 1) & 1u, timeout_ns, err) &&
+        ok = mbar_wait(k_full(b), (j >> 1) & 1u, timeout_ns, err) &&
              (j < 2 || mbar_wait(s_free(b), ((j - 2) >> 1) & 1u, timeout_ns, err));
         if (!ok) break;
         tc_fence_after();
@@ -247,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_tile;
       } else if (__any_sync(0xFFFFFFFFu, grow)) {
         const float m_new = fmaxf(m, m_tile);
-        const float alpha = exp2f(m - m_new);
+        const float alpha = fast_exp2(m - m_new);
         m = m_new;
         l *= alpha;
         // PV_{j-1} (written with the old max) must have landed in O first
@@ -271,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t packed[kBKV / 2];
 #pragma unroll
       for (int c = 0; c < kBKV; c += 2) {
-        const float p0 = exp2f(fmaf(s[c], scale_log2, -m));
-        const float p1 = exp2f(fmaf(s[c + 1], scale_log2, -m));
+        const float p0 = fast_exp2(fmaf(s[c], scale_log2, -m));
+        const float p1 = fast_exp2(fmaf(s[c + 1], scale_log2, -m));
         sum += p0 + p1;
         packed[c / 2] = pack_bf16x2(p0, p1);
       }
