@@ -257,13 +257,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free(b));
       const int kbase = j * kBKV;
-      float mx = -INFINITY;
+      if (kbase + kBKV > M) {  // the last tile may run past the keys
 #pragma unroll
-      for (int c = 0; c < kBKV; ++c) {
-        if (kbase + c >= M) s[c] = -INFINITY;
-        mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < kBKV; ++c)
+          if (kbase + c >= M) s[c] = -INFINITY;
       }
-      const float m_tile = mx * scale_log2;
+      // row max as a tree (8 independent chains)
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kBKV; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+#pragma unroll
+      for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + w]);
+      const float m_tile = mx8[0] * scale_log2;
       // rescale O when some row of the warp has a new max more than 2^8 above its old one
       const bool grow = m_tile > m + kRescaleThreshold;
       if (j == 0) {
@@ -290,16 +299,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
       }
       // p = 2^(s * scale_log2 - m), bf16 into P buffer b (128-byte swizzled row `row`)
-      float sum = 0.0f;
+      float sum8[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
       uint32_t packed[kBKV / 2];
 #pragma unroll
       for (int c = 0; c < kBKV; c += 2) {
         const float p0 = fast_exp2(fmaf(s[c], scale_log2, -m));
         const float p1 = fast_exp2(fmaf(s[c + 1], scale_log2, -m));
-        sum += p0 + p1;
+        sum8[(c >> 1) & 7] += p0 + p1;
         packed[c / 2] = pack_bf16x2(p0, p1);
       }
-      l += sum;
+#pragma unroll
+      for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) sum8[i] += sum8[i + w];
+      l += sum8[0];
       // the MMAs that read P buffer b last (PV_{j-2}) have completed
       if (j >= 2) {
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(pv_done(b), ((j - 2) >> 1) & 1u, timeout_ns, err));
