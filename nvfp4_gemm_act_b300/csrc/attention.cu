@@ -9,22 +9,23 @@
 //
 // Design: one CTA per (128-query tile, head), one CTA per SM (224 KB of shared memory).
 //   warp 0     TMA producer of Q (once: 4 boxes of 128 rows x 64 columns) and of the K tiles
-//              (4 boxes of 64 keys x 64) into a 2-stage ring; a K stage is free again as soon
-//              as the S MMAs that read it have completed;
+//              (4 boxes of 64 keys x 64) into a 3-stage ring; a K stage is free again as soon
+//              as the S MMAs that read it have completed. A K tile takes about 2,600 cycles
+//              from issue to arrival (measured), so it is fetched two tiles ahead of its use;
 //   warp 2     TMA producer of the V^T tiles (256 x 64 keys) into their own 2-stage ring; a V
-//              stage is free again when the PV MMAs that read it have completed. With the two
-//              rings released separately, K tiles are fetched about two tiles ahead of use;
-//   warp 1     TMEM allocation (512 columns: two 64-column S buffers, a 256-column O) and the
-//              MMA-issuing thread: S_j = Q K_j^T (M128 N64, 16 x K16), then O += P_{j-1} V_{j-1}
-//              (M128 N256, 4 x K16), so that the softmax of tile j runs while PV_{j-1} does;
+//              stage is free again when the PV MMAs that read it have completed;
+//   warp 1     TMEM allocation (512 columns: two 64-column S buffers, two 32-column P buffers,
+//              a 256-column O) and the MMA-issuing thread: S_j = Q K_j^T (M128 N64, 16 x K16,
+//              both operands in shared memory), then O += P_{j-1} V_{j-1} (M128 N256, 4 x K16,
+//              P read from TMEM), so that the softmax of tile j runs while PV_{j-1} does;
 //   warps 4-7  softmax, one query row per thread (TMEM lane = row): S from TMEM, running max
-//              in log2 units, p = 2^(s log2(e) / 16 - m) rounded to bf16 into a swizzled
-//              shared-memory P tile (the next MMA's A operand), running sum l in fp32. O is
+//              in log2 units, p = 2^(s log2(e) / 16 - m) rounded to bf16 and stored into the
+//              row's P buffer in TMEM (two bf16 per column), running sum l in fp32. O is
 //              rescaled (TMEM load, scale, store) only when a row's max grows by more than 8
 //              (a factor 256): until then p <= 256 and the stale max cancels in O / l.
 //              At the end O / l is written as bf16.
-// Every operand is K-major with the 128-byte swizzle: V is handed over transposed (V^T, keys
-// contiguous), written by a transpose kernel from the QKV output.
+// Every shared-memory operand is K-major with the 128-byte swizzle: V is handed over
+// transposed (V^T, keys contiguous), written by a transpose kernel from the QKV output.
 // Every wait is bounded (NVFP4_ERR_TIMEOUT in *err on expiry); a CTA that gives up drains
 // what it issued and frees TMEM before it exits.
 
@@ -43,25 +44,26 @@ namespace {
 constexpr int kHd = 256;            // head_dim
 constexpr int kBQ = 128;            // queries per CTA (TMEM lanes)
 constexpr int kBKV = 64;            // keys per tile
-constexpr int kStages = 2;          // K ring and V^T ring
+constexpr int kKStages = 3;         // K ring
+constexpr int kVStages = 2;         // V^T ring
 constexpr int kChunk = 64;          // bf16 elements in one 128-byte swizzle row
 constexpr int kQChunkBytes = kBQ * 128;        // 16 KB
 constexpr int kQBytes = (kHd / kChunk) * kQChunkBytes;   // 64 KB
 constexpr int kKChunkBytes = kBKV * 128;       // 8 KB
 constexpr int kKBytes = (kHd / kChunk) * kKChunkBytes;   // 32 KB
 constexpr int kVBytes = kHd * 128;             // 32 KB: 256 rows (d) x 64 keys
-constexpr int kStageBytes = kKBytes + kVBytes;   // K stage b, then V^T stage b
-constexpr int kPBytes = kBQ * 128;             // 16 KB: 128 rows x 64 keys
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kSmemBytes = kOffBar + 128 + 1024;   // barriers, TMEM slot, 1 KB alignment slack
+constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffV = kOffK + kKStages * kKBytes;
+constexpr int kOffBar = kOffV + kVStages * kVBytes;
+constexpr int kBarBytes = 256;                   // 18 barriers and the TMEM slot
+constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + 1 KB alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 constexpr int kThreads = 256;
 constexpr int kSoftWarp0 = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;       // S buffer b at columns [64 b, 64 b + 64)
+constexpr uint32_t kColP = 128;     // P buffer b at columns [128 + 32 b, 160 + 32 b): 64 bf16 a row
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 
@@ -82,6 +84,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
       "}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (fp32, TMEM) (+)= A B^T with A (bf16, M = 128 rows = TMEM lanes, two K-elements per
+// column) in TMEM and B in shared memory (kind::f16, K = 16 per instruction).
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -115,19 +130,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  // bars: [0] Q full; [1, 3) K stage full; [3, 5) S buffer full (MMA commit: S_j in TMEM,
-  // K stage free); [5, 7) S buffer read (4 softmax warps); [7, 9) P buffer written (4
-  // softmax warps); [9, 11) PV done with P buffer b (MMA commit: P buffer and V stage free,
-  // O updated); [11] drain; [12, 14) V stage full
+  // bars: [0] Q full; [1, 4) K stage full; [4, 7) K stage free (MMA commit after S);
+  // [7, 9) S buffer full (MMA commit); [9, 11) S buffer read (4 softmax warps); [11, 13) P
+  // buffer written (4 softmax warps); [13, 15) PV done with P buffer b (MMA commit: P buffer
+  // and V stage free, O updated); [15, 17) V stage full; [17] drain
   const uint32_t q_full = smem_u32(bars);
   auto k_full = [&](int b) { return smem_u32(bars + 1 + b); };
-  auto s_full = [&](int b) { return smem_u32(bars + 3 + b); };
-  auto s_free = [&](int b) { return smem_u32(bars + 5 + b); };
-  auto p_full = [&](int b) { return smem_u32(bars + 7 + b); };
-  auto pv_done = [&](int b) { return smem_u32(bars + 9 + b); };
-  const uint32_t drain_bar = smem_u32(bars + 11);
-  auto v_full = [&](int b) { return smem_u32(bars + 12 + b); };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  auto k_free = [&](int b) { return smem_u32(bars + 4 + b); };
+  auto s_full = [&](int b) { return smem_u32(bars + 7 + b); };
+  auto s_free = [&](int b) { return smem_u32(bars + 9 + b); };
+  auto p_full = [&](int b) { return smem_u32(bars + 11 + b); };
+  auto pv_done = [&](int b) { return smem_u32(bars + 13 + b); };
+  auto v_full = [&](int b) { return smem_u32(bars + 15 + b); };
+  const uint32_t drain_bar = smem_u32(bars + 17);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  static_assert(19 * 8 <= kBarBytes, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -140,8 +157,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_vt);
     mbar_init(q_full, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kKStages; ++b) {
       mbar_init(k_full(b), 1);
+      mbar_init(k_free(b), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(v_full(b), 1);
       mbar_init(s_full(b), 1);
       mbar_init(s_free(b), 4);
@@ -171,27 +191,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sbase + kOffQ + c * kQChunkBytes, &tm_q, head * kHd + c * kChunk, q0, q_full, pol);
       }
       const int kcol = hidden + head * kHd;
+      const int stages = kpart ? kKStages : kVStages;
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
-        const int b = j & 1;
-        // the stage's previous tile (j - 2) has been read: by S_{j-2} (K) or PV_{j-2} (V)
-        if (j >= 2 && !mbar_wait(kpart ? s_full(b) : pv_done(b), ((j - 2) >> 1) & 1u, timeout_ns, err)) break;
-        const uint32_t stage = sbase + kOffKV + b * kStageBytes;
+        const int b = j % stages;
+        const uint32_t use = static_cast<uint32_t>(j / stages);  // this stage's use count
+        // the stage's previous tile has been read: by its S MMAs (K) or its PV MMAs (V)
+        if (j >= stages &&
+            !mbar_wait(kpart ? k_free(b) : pv_done(b), (use - 1u) & 1u, timeout_ns, err))
+          break;
         if (kpart) {
+          const uint32_t stage = sbase + kOffK + b * kKBytes;
           mbar_arrive_expect_tx(k_full(b), kKBytes);
           for (int c = 0; c < kHd / kChunk; ++c)
             tma_load_2d(stage + c * kKChunkBytes, &tm_k, kcol + c * kChunk, j * kBKV, k_full(b), pol);
         } else {
           mbar_arrive_expect_tx(v_full(b), kVBytes);
-          tma_load_2d(stage + kKBytes, &tm_vt, j * kBKV, head * kHd, v_full(b), pol);
+          tma_load_2d(sbase + kOffV + b * kVBytes, &tm_vt, j * kBKV, head * kHd, v_full(b), pol);
         }
         issued = j + 1;
       }
-      // No copy may still be in flight when the CTA exits: the last two stages' loads (the
+      // No copy may still be in flight when the CTA exits: the last loads of every stage (the
       // earlier ones were waited for before their stage was reused) and the Q tile.
       if (kpart) (void)mbar_wait(q_full, 0u, timeout_ns, err);
-      for (int j = issued >= 2 ? issued - 2 : 0; j < issued; ++j)
-        (void)mbar_wait(kpart ? k_full(j & 1) : v_full(j & 1), (j >> 1) & 1u, timeout_ns, err);
+      for (int j = issued >= stages ? issued - stages : 0; j < issued; ++j)
+        (void)mbar_wait(kpart ? k_full(j % stages) : v_full(j % stages), static_cast<uint32_t>(j / stages) & 1u,
+                        timeout_ns, err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -203,22 +228,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait(p_full(b), (i >> 1) & 1u, timeout_ns, err))
           return false;
         tc_fence_after();
-        const uint32_t p_s = sbase + kOffP + b * kPBytes;
-        const uint32_t v_s = sbase + kOffKV + b * kStageBytes + kKBytes;
+        const uint32_t v_s = sbase + kOffV + b * kVBytes;
 #pragma unroll
         for (int k = 0; k < kBKV / 16; ++k)
-          mma_bf16(tmem_base + kColO, kmajor_desc(p_s + k * 32), kmajor_desc(v_s + k * 32), kIdescO,
-                   (i | k) != 0 ? 1u : 0u);
+          mma_bf16_tmem_a(tmem_base + kColO, tmem_base + kColP + b * (kBKV / 2) + k * 8, kmajor_desc(v_s + k * 32),
+                          kIdescO, (i | k) != 0 ? 1u : 0u);
         tc_commit(pv_done(b));
         return true;
       };
       for (int j = 0; j < nt && ok; ++j) {
         const int b = j & 1;
-        ok = mbar_wait(k_full(b), (j >> 1) & 1u, timeout_ns, err) &&
+        const int kb = j % kKStages;
+        ok = mbar_wait(k_full(kb), static_cast<uint32_t>(j / kKStages) & 1u, timeout_ns, err) &&
              (j < 2 || mbar_wait(s_free(b), ((j - 2) >> 1) & 1u, timeout_ns, err));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t k_s = sbase + kOffKV + b * kStageBytes;
+        const uint32_t k_s = sbase + kOffK + kb * kKBytes;
 #pragma unroll
         for (int c = 0; c < kHd / kChunk; ++c)
 #pragma unroll
@@ -226,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_bf16(tmem_base + kColS + b * kBKV, kmajor_desc(sbase + kOffQ + c * kQChunkBytes + k * 32),
                      kmajor_desc(k_s + c * kKChunkBytes + k * 32), kIdescS, (c | k) != 0 ? 1u : 0u);
         tc_commit(s_full(b));
+        tc_commit(k_free(kb));
         if (j >= 1) ok = issue_pv(j - 1);
       }
       if (ok) (void)issue_pv(nt - 1);
@@ -318,12 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(pv_done(b), ((j - 2) >> 1) & 1u, timeout_ns, err));
         if (!ok) break;
       }
-      uint8_t* prow = smem + kOffP + b * kPBytes + row * 128;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
-            make_uint4(packed[4 * u], packed[4 * u + 1], packed[4 * u + 2], packed[4 * u + 3]);
-      fence_proxy_async_smem();
+      tmem_st_32cols(lane_addr + kColP + b * (kBKV / 2), packed);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(b));
     }
