@@ -1,7 +1,8 @@
 """One DiT block's linears chained on the GPU, attention between the first two:
 
   x -> quantize -> QKV GEMM + bias + per-head RMSNorm of Q and K (bf16)
-    -> attention over all tokens (a torch op, scaled dot-product attention)
+    -> attention over all tokens (this package's attention kernel; torch's
+       scaled_dot_product_attention with attention_impl="torch")
     -> quantize -> output-projection GEMM + bias (bf16)
     -> quantize -> gated up-projection GEMM, SiLU(gate) * up, written as NVFP4 (static scale)
     -> down-projection GEMM + bias (bf16)
@@ -13,7 +14,7 @@ the sum of its layers. The up-projection hands the down-projection NVFP4 directl
 widest activation never round-trips through HBM in bf16. Residual connections and the
 timestep modulation of a full DiT block are not part of that path and are left out.
 
-Every GEMM, epilogue and quantizer runs in this package's kernels; attention is torch's.
+Every GEMM, epilogue, quantizer and (by default) the attention runs in this package's kernels.
 """
 from __future__ import annotations
 
@@ -37,7 +38,7 @@ class DitBlockLinears:
     """
 
     def __init__(self, w_qkv, b_qkv, gamma, w_o, b_o, w_up, b_up, w_down, b_down, heads: int,
-                 head_dim: int = 256, eps: float = 1e-6, device="cuda:0", attention_impl: str = "torch"):
+                 head_dim: int = 256, eps: float = 1e-6, device="cuda:0", attention_impl: str = "kernel"):
         assert attention_impl in ("kernel", "torch")
         self.attention_impl = attention_impl
         self.heads, self.head_dim, self.eps = heads, head_dim, eps
@@ -134,7 +135,7 @@ class DitBlockLinears:
 
 
 def seeded_dit_block(M: int = 4608, device="cuda:0", seed: Optional[int] = None,
-                     heads: int = W.DIT_HEADS, mlp: int = 12288, attention_impl: str = "torch"):
+                     heads: int = W.DIT_HEADS, mlp: int = 12288, attention_impl: str = "kernel"):
     """The seeded synthetic block (random-initialised weights of the four layers, drawn by
     ``workloads.dit_block``) on ``device``, and its bf16 input [M, heads * 256]."""
     qkv, o, up, down = W.dit_block(M, seed, heads=heads, mlp=mlp)

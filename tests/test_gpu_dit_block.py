@@ -1,14 +1,16 @@
-"""GPU parity of one DiT block's chained linears (DitBlockLinears, attention by torch) against
-the oracle's chained block, on the same seeded inputs and the same static up-projection scale
-(the oracle's calibration value, handed to the GPU block).
+"""GPU parity of one DiT block's chained linears (DitBlockLinears, with this package's attention
+kernel between the first two) against the oracle's chained block, on the same seeded inputs
+and the same static up-projection scale (the oracle's calibration value, handed to the GPU
+block).
 
 What is compared, stage by stage:
   * QKV + per-head RMSNorm: the established bf16 bar (RN_bf16 of the oracle value or a
     neighbour), since both sides start from identical quantized operands;
-  * attention: torch's bf16 attention against the oracle's fp64 softmax attention of the
-    oracle's QKV output. Rounding the probabilities to bf16 (relative 2^-9 each) gives an
-    output error of about 2^-9 * rms(v) / sqrt(effective keys), ~2e-3 of the output's RMS
-    here; the bound is 5e-3 of the RMS, and 0.1 of the RMS for the largest element;
+  * attention: the attention kernel (bf16 probabilities, fp32 accumulation) against the
+    oracle's fp64 softmax attention of the oracle's QKV output. Rounding the probabilities to
+    bf16 (relative 2^-9 each) gives an output error of about 2^-9 * rms(v) / sqrt(effective
+    keys), ~2e-3 of the output's RMS here; the bound is 5e-3 of the RMS, and 0.1 of the RMS
+    for the largest element;
   * the later stages quantize their inputs again: a value within rounding error of a code or
     block-scale boundary can round either way, and such differences grow through three more
     quantizations. What is fixed is that both chains carry the same quantization error against
