@@ -493,7 +493,7 @@ def _linear_ref(x, w, bias, epilogue, quantized, gamma=None, head_dim=256, norm_
 
 
 def dit_block_ref(x, layers, heads: int, head_dim: int, eps: float = 1e-6, ts_mid=None,
-                  quantized: bool = True):
+                  quantized: bool = True, rows=None):
     """One DiT block's linears with attention between the first two, in the order of the page
     "How fal made Ideogram V4 6x faster" (each large GEMM followed by its small op, fused).
 
@@ -511,7 +511,12 @@ def dit_block_ref(x, layers, heads: int, head_dim: int, eps: float = 1e-6, ts_mi
          ``ts_mid`` if given, else amax(u) / 2688 (the static scale a calibration pass sets)
       6. y = bf16(quant(u; ts_mid) W_down + b_down)
     ``quantized`` False: every quantization and bf16 rounding dropped, the exact fp64 function
-    the quantized block approximates. Returns (y, dict of the intermediates and ts_mid).
+    the quantized block approximates. ``rows`` (token indices): the output of those tokens
+    only; every token's K and V still enter the attention, and the dynamic scales of the
+    quantized block's activations are still those of all tokens, so the stages that feed a
+    dynamic scale run over all tokens and the last two layers over ``rows`` (the default
+    ts_mid is then amax / 2688 over those rows). Returns (y, dict of the intermediates, for
+    all tokens or for ``rows`` where a stage ran only there, and ts_mid).
     """
     hidden = heads * head_dim
     rnd = round_to_bf16 if quantized else (lambda z: np.asarray(z, np.float64))
@@ -520,9 +525,15 @@ def dit_block_ref(x, layers, heads: int, head_dim: int, eps: float = 1e-6, ts_mi
     t = rnd(_linear_ref(x, w1, b1, EPI_HEAD_RMSNORM, quantized, gamma=g1, head_dim=head_dim,
                         norm_cols=2 * hidden, eps=eps))
     qkv = t.reshape(M, 3, heads, head_dim).transpose(1, 2, 0, 3)    # [3, heads, M, head_dim]
-    a = rnd(attention_ref(qkv[0], qkv[1], qkv[2]).transpose(1, 0, 2).reshape(M, hidden))
+    q_rows = qkv[0] if (rows is None or quantized) else qkv[0][:, rows]
+    a = rnd(attention_ref(q_rows, qkv[1], qkv[2]).transpose(1, 0, 2).reshape(-1, hidden))
     o = rnd(_linear_ref(a, w2, b2, EPI_BIAS, quantized))
-    u = rnd(_linear_ref(o, w3, b3, EPI_GATED_SILU, quantized))
+    o_ts = tensor_scale_ref(o) if quantized else None
+    if rows is not None and quantized:
+        o_in = o[rows]
+    else:
+        o_in = o
+    u = rnd(_linear_ref(o_in, w3, b3, EPI_GATED_SILU, quantized, tensor_scale=o_ts))
     if quantized and ts_mid is None:
         ts_mid = tensor_scale_ref(u)
     y = rnd(_linear_ref(u, w4, b4, EPI_BIAS, quantized, tensor_scale=ts_mid))

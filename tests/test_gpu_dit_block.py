@@ -114,3 +114,38 @@ def test_calibrated_static_scale(block):
     # oracle's: one extreme value of a chain whose stages differ by rounding
     ts_ref = float(block["ref"]["ts_mid"])
     assert abs(block["ts_gpu"] / ts_ref - 1.0) <= 0.05
+
+
+def test_full_size_block_sampled_rows():
+    # the benchmarked shape: 4608 tokens through the full-width block, 16 sampled output rows
+    # (every token's K and V and every dynamic scale still come from all tokens)
+    M, seed = 4608, 70
+    ls = W.dit_block(M, seed)
+    x = W.make_x(ls[0])
+    layers = []
+    for w in ls:
+        b, g = W.make_bias(w), W.make_gamma(w)
+        layers.append((W.make_w(w).float().numpy(), None if b is None else b.double().numpy(),
+                       None if g is None else g.double().numpy()))
+    rows = np.unique(np.concatenate([[0, 255, 256, M - 1], np.random.default_rng(71).integers(0, M, 12)]))
+    xs = x.float().numpy()
+    y_ref, ref = R.dit_block_ref(xs, layers, 12, 256, rows=rows)
+    y_ex, ex = R.dit_block_ref(xs, layers, 12, 256, quantized=False, rows=rows)
+    blk, xd = seeded_dit_block(M, DEV, seed=seed)
+    blk.calibrate(xd, ts_mid=torch.tensor([ref["ts_mid"]], dtype=torch.float32, device=DEV))
+    keep = {}
+    y = to_np_f32(blk(xd, keep=keep)).astype(np.float64)[rows]
+    torch.cuda.synchronize()
+    assert_bf16_close(to_np_f32(keep["qkv_rmsnorm"])[rows], ref["qkv"][rows], "full block qkv rows")
+    a = to_np_f32(keep["attention"]).astype(np.float64)[rows]
+    a_ref = ref["attention"][rows]
+    assert _rel(a, a_ref) <= 5e-3
+    assert float(np.abs(a - a_ref).max()) <= 0.1 * float(np.sqrt(np.mean(a_ref ** 2)))
+    o = to_np_f32(keep["out_proj"]).astype(np.float64)[rows]
+    q_err_o = _rel(ref["out_proj"][rows], ex["out_proj"])
+    assert _rel(o, ex["out_proj"]) <= 1.02 * q_err_o
+    assert _rel(o, ref["out_proj"][rows]) <= 0.15 * q_err_o
+    assert np.all(np.isfinite(y))
+    q_err = _rel(y_ref, y_ex)
+    assert _rel(y, y_ex) <= 1.02 * q_err, (_rel(y, y_ex), q_err)
+    assert _rel(y, y_ref) <= 0.5 * q_err, (_rel(y, y_ref), q_err)

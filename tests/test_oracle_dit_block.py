@@ -152,3 +152,15 @@ def test_block_static_scale_and_exact_limit():
     t = ei["qkv"]
     qk = (t[:, :2 * H] / layers[0][2][None, :]).reshape(M, 2 * HEADS, HD)
     np.testing.assert_allclose(np.mean(qk ** 2, axis=2), 1.0, rtol=1e-4)
+
+
+def test_block_sampled_rows_equal_the_full_block_rows():
+    # the sampled-rows form computes the same numbers for those tokens as the full block
+    x, layers = _block(12)
+    rows = np.array([0, 3, 7, 11])
+    y, inter = R.dit_block_ref(x, layers, HEADS, HD)
+    ys, _ = R.dit_block_ref(x, layers, HEADS, HD, ts_mid=inter["ts_mid"], rows=rows)
+    assert np.array_equal(ys, y[rows])
+    ye, _ = R.dit_block_ref(x, layers, HEADS, HD, quantized=False)
+    yes, _ = R.dit_block_ref(x, layers, HEADS, HD, quantized=False, rows=rows)
+    np.testing.assert_allclose(yes, ye[rows], rtol=1e-12, atol=1e-13)
