@@ -10,8 +10,9 @@
 // Design: one CTA per (128-query tile, head), one CTA per SM (224 KB of shared memory).
 //   warp 0     TMA producer of Q (once: 4 boxes of 128 rows x 64 columns) and of the K tiles
 //              (4 boxes of 64 keys x 64) into a 3-stage ring; a K stage is free again as soon
-//              as the S MMAs that read it have completed. A K tile takes about 2,600 cycles
-//              from issue to arrival (measured), so it is fetched two tiles ahead of its use;
+//              as the S MMAs that read it have completed, so a K tile is requested two tiles
+//              ahead of its use (K and V^T tiles take 2,600-4,400 cycles to arrive, measured:
+//              each SM takes them in at ~33 bytes a cycle);
 //   warp 2     TMA producer of the V^T tiles (256 x 64 keys) into their own 2-stage ring; a V
 //              stage is free again when the PV MMAs that read it have completed;
 //   warp 1     TMEM allocation (512 columns: two 64-column S buffers, two 32-column P buffers,

@@ -51,11 +51,30 @@ def _check(got, ref, what):
 
 
 @pytest.mark.parametrize("M,heads,q_scale", [(200, 2, 1.0), (1, 1, 1.0), (64, 1, 1.0), (65, 1, 1.0),
-                                             (384, 4, 1.0), (300, 2, 4.0), (700, 1, 8.0)])
+                                             (384, 4, 1.0), (300, 2, 4.0), (700, 1, 8.0), (1000, 3, 1.0)])
 def test_attention_matches_oracle(M, heads, q_scale):
     qkv = W.attention_qkv(M, heads, seed=M + heads, q_scale=q_scale)
     got = _run(qkv, heads)
     _check(got, _ref(to_np_f32(qkv).astype(np.float64), heads), f"M={M} heads={heads} q x{q_scale}")
+
+
+def test_attention_strided_input_and_output():
+    # qkv and out as column windows of wider buffers (row pitches 3 H + 64 and H + 128)
+    M, heads = 200, 2
+    H = heads * HD
+    qkv = W.attention_qkv(M, heads, seed=12)
+    wide = torch.zeros((M, 3 * H + 64), dtype=torch.bfloat16)
+    wide[:, 32:32 + 3 * H] = qkv
+    src = wide.to(DEV)[:, 32:32 + 3 * H]
+    big_out = torch.full((M, H + 128), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = big_out[:, 64:64 + H]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    nv.attention(src, heads, out=out, device_error=err)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_device_error(err) == 0
+    _check(to_np_f32(out).astype(np.float64), _ref(to_np_f32(qkv).astype(np.float64), heads), "strided")
+    # nothing outside the output window was written
+    assert bool((big_out[:, :64] == 7.0).all()) and bool((big_out[:, 64 + H:] == 7.0).all())
 
 
 def test_attention_single_token_returns_v():
