@@ -80,7 +80,13 @@ def _check(func: str, status: int) -> None:
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else t.data_ptr()
+    """Device address of a CUDA tensor (every tensor the library reads or writes is device
+    memory: a host tensor's address would be dereferenced by a kernel)."""
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("nvfp4_gemm_act_b300: expected a CUDA tensor, got one on " + str(t.device))
+    return t.data_ptr()
 
 
 def _stream(stream=None):

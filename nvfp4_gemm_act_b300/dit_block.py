@@ -49,6 +49,7 @@ class DitBlockLinears:
         assert w_up.shape == (h, 2 * m) and w_down.shape == (m, h)
         assert gamma is not None and gamma.numel() == 2 * h
         dev = torch.device(device)
+        self.device = dev
 
         def put(t):
             return None if t is None else t.to(dev)
@@ -99,7 +100,7 @@ class DitBlockLinears:
             o = self.out_proj(self.attention(self.qkv_rmsnorm(x)))
             u = nvfp4_gemm(nvfp4_quantize(o), self.qb["up"], "gated_silu", bias=self.bias["up"])
             ts_mid = (u.float().abs().max() / 2688.0).reshape(1)
-        self.ts_mid = ts_mid.to(torch.float32).reshape(1).contiguous()
+        self.ts_mid = ts_mid.to(self.device, torch.float32).reshape(1).contiguous()
         return self.ts_mid
 
     def forward(self, x: torch.Tensor, timings: Optional[Dict[str, List[float]]] = None,

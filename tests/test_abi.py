@@ -229,3 +229,14 @@ def test_valid_arguments_without_a_gpu_report_the_device():
     assert nv.lib().fp8_quantize(FAKE, 128, 128, 128, FAKE, FAKE, None, FAKE, None) == ERR_DEVICE
     assert nv.lib().fp8_pack_weights(FAKE, 256, 256, 0, FAKE, FAKE, FAKE, None) == ERR_DEVICE
     assert nv.lib().nvfp4_debug_wait_timeout(FAKE, 1000, None) == ERR_DEVICE
+
+
+def test_binding_refuses_host_tensors():
+    # a host tensor's address must never reach a kernel: the binding refuses it before any call
+    x = torch.zeros((128, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        nv.nvfp4_quantize(x)
+    with pytest.raises(ValueError):
+        nv.fp8_quantize(x)
+    with pytest.raises(ValueError):
+        nv.attention(torch.zeros((64, 3 * 256), dtype=torch.bfloat16), 1)
