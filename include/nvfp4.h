@@ -32,10 +32,10 @@
  *     on-chip resources and ends the kernel; the output is then undefined.
  *   - Non-finite inputs (inf, NaN) are outside the format; their results are undefined.
  *   - Requires a compute capability 10.3 GPU (B300); others get NVFP4_ERR_DEVICE.
- *   - One device per process: each kernel's launch attributes (its shared-memory size) are
- *     set once, on the device current at the first call; a call on another device of the
- *     same process then fails with NVFP4_ERR_LAUNCH (run one process per GPU, as the
- *     multi-GPU replicas do).
+ *   - One device per process: each kernel's launch attributes (its shared-memory size) and
+ *     occupancy figures are set up once, with the device current at the first call; calls
+ *     on another device of the same process are not supported (run one process per GPU,
+ *     as the multi-GPU replicas do).
  *   - The FP8 and attention calls below follow the same conventions.
  */
 #ifndef NVFP4_H_
