@@ -815,13 +815,25 @@ def run_dit_block(args):
                 times.setdefault(k, []).extend(v)
             total.append(ms_total)
     assert bool(torch.isfinite(y.float()).all())
+    # the same block replayed as one CUDA graph (no per-launch host work between stages)
+    replay, _ = blk.graph(x)
+    graph_ms = []
+    for it in range(max(args.warmup, 3) + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if it >= max(args.warmup, 3):
+            graph_ms.append(e0.elapsed_time(e1))
     h, m = blk.hidden, blk.mlp
     flops = {"qkv_rmsnorm": 2 * M * h * 3 * h, "attention": 4 * M * M * h, "out_proj": 2 * M * h * h,
              "up_gated_silu": 2 * M * h * 2 * m, "down": 2 * M * m * h}
     ms = {k: round(float(np.median(times[k])), 5) for k in STAGES}
     tot = float(np.median(total))
     print(json.dumps({"dit_block": f"M={M} hidden={h} heads={blk.heads}x{blk.head_dim} mlp={m}",
-                      "total_ms": round(tot, 5), "ms": ms,
+                      "total_ms": round(tot, 5), "graph_total_ms": round(float(np.median(graph_ms)), 5), "ms": ms,
                       "share": {k: round(v / sum(ms.values()), 4) for k, v in ms.items()},
                       "tflops": {k: round(flops[k] / (ms[k] / 1e3) / 1e12, 1) for k in STAGES},
                       "nvfp4_gemm_tflops_block": round(blk.gemm_flops(M) / ((tot - ms["attention"]) / 1e3) / 1e12, 1),

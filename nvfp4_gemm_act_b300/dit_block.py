@@ -130,6 +130,23 @@ class DitBlockLinears:
 
     __call__ = forward
 
+    def graph(self, x: torch.Tensor):
+        """The forward pass on the device buffer ``x`` captured once as a CUDA graph (after one
+        eager pass, which also sets up every kernel's launch attributes). Returns (replay, y):
+        ``replay()`` re-runs the whole block on the current contents of ``x`` with one graph
+        launch and writes the result into ``y``."""
+        if self.ts_mid is None:
+            raise RuntimeError("DitBlockLinears: calibrate() sets the up-projection's output scale first")
+        side = torch.cuda.Stream(device=x.device)
+        side.wait_stream(torch.cuda.current_stream(x.device))
+        with torch.cuda.stream(side):
+            self.forward(x)
+        torch.cuda.current_stream(x.device).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            y = self.forward(x)
+        return g.replay, y
+
     def gemm_flops(self, M: int) -> int:
         h, m = self.hidden, self.mlp
         return 2 * M * h * (3 * h + h + 2 * m) + 2 * M * m * h

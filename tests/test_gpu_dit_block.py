@@ -149,3 +149,21 @@ def test_full_size_block_sampled_rows():
     q_err = _rel(y_ref, y_ex)
     assert _rel(y, y_ex) <= 1.02 * q_err, (_rel(y, y_ex), q_err)
     assert _rel(y, y_ref) <= 0.5 * q_err, (_rel(y, y_ref), q_err)
+
+
+def test_cuda_graph_replay_matches_eager():
+    # the whole block as one CUDA graph: the same kernels on the same inputs, so the same bytes
+    blk, xd = seeded_dit_block(384, DEV, seed=72, heads=4, mlp=4096)
+    blk.calibrate(xd)
+    y_eager = blk(xd).clone()
+    replay, y_graph = blk.graph(xd)
+    replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y_graph, y_eager)
+    # a new input in the captured buffer gives that input's result
+    x2 = torch.randn_like(xd.float()).to(torch.bfloat16)
+    y2_eager = blk(x2).clone()
+    xd.copy_(x2)
+    replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y_graph, y2_eager)
