@@ -39,3 +39,27 @@ def test_sweep_covers_three_gemms_at_five_sizes():
     assert len(s) == 15
     assert sorted({w.M for w in s}) == list(W.SWEEP_M)
     assert {w.seed for w in s} == set(range(10, 15))
+
+
+def test_dit_block_layers_chain():
+    # each layer's K is the previous stage's output width; the narrow variant keeps head_dim 256
+    for heads, mlp in ((12, 12288), (4, 4096)):
+        qkv, o, up, down = W.dit_block(384, seed=5, heads=heads, mlp=mlp)
+        h = heads * 256
+        assert (qkv.K, qkv.N, qkv.norm_cols, qkv.head_dim) == (h, 3 * h, 2 * h, 256)
+        assert (o.K, o.N) == (h, h)
+        assert (up.K, up.N, up.out_cols) == (h, 2 * mlp, mlp)
+        assert (down.K, down.N) == (mlp, h)
+        assert all(w.M == 384 for w in (qkv, o, up, down))
+    # the full-width block reuses the benchmark layers' weights (same seeds)
+    full = W.dit_block(4608)
+    assert torch.equal(W.make_w(full[2]), W.make_w(W.GATED_UP))
+
+
+def test_attention_qkv_is_seeded_and_scales_only_q():
+    a = W.attention_qkv(16, 2, seed=3)
+    b = W.attention_qkv(16, 2, seed=3, q_scale=4.0)
+    assert a.shape == (16, 3 * 512) and a.dtype == torch.bfloat16
+    assert torch.equal(a, W.attention_qkv(16, 2, seed=3))
+    assert torch.equal(a[:, 512:], b[:, 512:])
+    assert not torch.equal(a[:, :512], b[:, :512])
