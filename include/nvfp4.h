@@ -27,6 +27,11 @@
  *     nvfp4_get_device_error.
  *   - Host-side checks run before anything is launched; a failed check returns a non-zero
  *     status and launches nothing. A launch failure returns NVFP4_ERR_LAUNCH.
+ *   - Every pointer a call reads or writes must be memory of the CURRENT device (cudaMalloc'd
+ *     there, or managed memory associated with it). Host memory (pageable or pinned) and
+ *     another GPU's memory reached through unified addressing are refused with
+ *     NVFP4_ERR_ARG before anything is launched: no kernel of the library, and no TMA tensor
+ *     map it encodes, ever covers another device's memory.
  *   - Device-side waits are bounded in time. A wait that runs out writes
  *     NVFP4_ERR_TIMEOUT into *device_error (when device_error is not NULL), frees its
  *     on-chip resources and ends the kernel; the output is then undefined.
@@ -34,8 +39,7 @@
  *   - Requires a compute capability 10.3 GPU (B300); others get NVFP4_ERR_DEVICE.
  *   - One device per process: each kernel's launch attributes (its shared-memory size) and
  *     occupancy figures are set up once, with the device current at the first call; calls
- *     on another device of the same process are not supported (run one process per GPU,
- *     as the multi-GPU replicas do).
+ *     on another device of the same process are not supported (run one process per GPU).
  *   - The FP8 and attention calls below follow the same conventions.
  */
 #ifndef NVFP4_H_
@@ -319,16 +323,17 @@ NVFP4_API nvfp4_status nvfp4_debug_wait_timeout(int *device_error, int64_t timeo
  * must not call cudaMalloc/cudaFree, because those can synchronize the device or fail for
  * lack of memory in the middle of a request.
  *
- * Arguments and results are those of nvfp4_quantize with tensor_scale_in = NULL. The
- * scratch (the amax word and a finished-CTA count) is a fixed 256-byte array inside the
- * library, resident on every GPU that loads it until the process exits; the quantizer
- * needs 16 bytes of it, and a need above 256 bytes would be refused with NVFP4_ERR_SHAPE.
- * Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine is called.
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current) and caches it; make that first call before any stream
- * capture. Every call shares the array and zeroes the 16 bytes it uses on `stream` before
- * the quantizer runs, so calls that overlap on the GPU (different streams, or different
- * host threads) race: serialize them.
+ * Arguments, checks and results are those of nvfp4_quantize with tensor_scale_in = NULL;
+ * every check runs first, so a refused call touches neither the scratch nor the stream.
+ * The scratch (the quantizer's 16 workspace bytes: the amax word, two grid-barrier counters
+ * and a failure flag) is a fixed 256-byte array inside the library, resident on every GPU
+ * that loads it until the process exits; a need above 256 bytes would be refused with
+ * NVFP4_ERR_SHAPE. Nothing is allocated: no cudaMalloc, cudaFree or allocating library
+ * routine is called. The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that first call
+ * before any stream capture. Every call shares the array and zeroes the 16 bytes it uses on
+ * `stream` before the quantizer runs, so calls that overlap on the GPU (different streams,
+ * or different host threads) race: serialize them.
  */
 NVFP4_API nvfp4_status nvfp4_quantize_noalloc(const void *x, int64_t M, int64_t K, int64_t ldx,
                                               uint8_t *codes, uint8_t *scales,

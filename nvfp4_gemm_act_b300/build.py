@@ -13,7 +13,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libnvfp4.so")
 SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "attention.cu", "noalloc.cu"]
-HEADERS = ["nvfp4_device.cuh", "nvfp4_internal.h"]
+HEADERS = ["nvfp4_device.cuh", "nvfp4_internal.h", "pointer_check.h"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

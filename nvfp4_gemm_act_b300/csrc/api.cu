@@ -5,10 +5,12 @@
 
 #include <atomic>
 #include <cstdlib>
+#include <initializer_list>
 #include <mutex>
 
 #include "../../include/nvfp4.h"
 #include "nvfp4_internal.h"
+#include "pointer_check.h"
 
 namespace nvfp4 {
 
@@ -74,7 +76,48 @@ nvfp4_status check_device() {
 
 nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH; }
 
+// Every non-NULL pointer of the list names memory of the current device (classify_pointer);
+// runs after check_device, before anything is launched.
+nvfp4_status check_pointers(std::initializer_list<const void*> ptrs) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return NVFP4_ERR_DEVICE;
+  }
+  for (const void* p : ptrs) {
+    if (p == nullptr) continue;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return NVFP4_ERR_ARG;
+    }
+    if (nvfp4_status st = nvfp4::classify_pointer(at.type, at.device, dev); st != NVFP4_OK) return st;
+  }
+  return NVFP4_OK;
+}
+
 }  // namespace
+
+namespace nvfp4 {
+
+nvfp4_status check_quantize_args(const void* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* codes,
+                                 const uint8_t* scales, const float* tensor_scale, const float* tensor_scale_in,
+                                 const void* workspace, bool library_scratch) {
+  if (M < 0 || K <= 0 || K % 64 != 0 || ldx < K) return NVFP4_ERR_SHAPE;
+  if (M > 0 && K > kMaxElems / M) return NVFP4_ERR_SHAPE;
+  if (M == 0) return NVFP4_OK;  // empty: nothing is read or written (pointers may be NULL)
+  if (x == nullptr || codes == nullptr || scales == nullptr || tensor_scale == nullptr)
+    return NVFP4_ERR_NULL;
+  if (!library_scratch && tensor_scale_in == nullptr && workspace == nullptr) return NVFP4_ERR_NULL;
+  if (!aligned16(x) || ldx % 8 != 0 || !aligned16(codes) || !aligned16(scales) ||
+      (workspace != nullptr && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
+    return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  return check_pointers({x, codes, scales, tensor_scale, tensor_scale_in, workspace});
+}
+
+}  // namespace nvfp4
 
 extern "C" {
 
@@ -107,17 +150,10 @@ const char* nvfp4_status_string(nvfp4_status s) {
 nvfp4_status nvfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                             uint8_t* scales, float* tensor_scale, const float* tensor_scale_in,
                             void* workspace, nvfp4_stream_t stream) {
-  if (M < 0 || K <= 0 || K % 64 != 0 || ldx < K) return NVFP4_ERR_SHAPE;
-  if (M > 0 && K > kMaxElems / M) return NVFP4_ERR_SHAPE;
-  if (M == 0) return NVFP4_OK;  // empty: nothing is read or written (pointers may be NULL)
-  if (x == nullptr || codes == nullptr || scales == nullptr || tensor_scale == nullptr)
-    return NVFP4_ERR_NULL;
-  if (tensor_scale_in == nullptr && workspace == nullptr) return NVFP4_ERR_NULL;
-  if (!aligned16(x) || ldx % 8 != 0 || !aligned16(codes) || !aligned16(scales) ||
-      (workspace != nullptr && !aligned16(workspace)) ||
-      (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
-    return NVFP4_ERR_ALIGN;
-  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  if (nvfp4_status st = nvfp4::check_quantize_args(x, M, K, ldx, codes, scales, tensor_scale, tensor_scale_in,
+                                                   workspace, false);
+      st != NVFP4_OK || M == 0)
+    return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return from_cuda(nvfp4::launch_quantize(x, M, K, ldx, codes, scales, static_cast<unsigned*>(workspace),
                                           tensor_scale_in, tensor_scale, s));
@@ -134,6 +170,7 @@ nvfp4_status nvfp4_pack_weights(const void* w, int64_t K, int64_t N, int gated_i
       (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
     return NVFP4_ERR_ALIGN;
   if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  if (nvfp4_status st = check_pointers({w, codes, scales, tensor_scale, workspace}); st != NVFP4_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   unsigned* amax = static_cast<unsigned*>(workspace);
   if (cudaMemsetAsync(amax, 0, nvfp4_workspace_bytes(), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
@@ -196,6 +233,14 @@ nvfp4_status gemm_inputs_ok(const nvfp4::GemmArgs& a) {
   return NVFP4_OK;
 }
 
+// Device check, then every pointer the GEMM kernel will read or write (tensor maps included)
+// must be memory of the current device.
+nvfp4_status gemm_memory_ok(const nvfp4::GemmArgs& a) {
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  return check_pointers({a.a_codes, a.a_scales, a.a_ts, a.b_codes, a.b_scales, a.b_ts, a.bias, a.gamma, a.out,
+                         a.out_codes, a.out_scales, a.out_ts, a.err});
+}
+
 }  // namespace
 
 nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const float* a_ts,
@@ -215,10 +260,10 @@ nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const f
   if (nvfp4_status st = gemm_inputs_ok(a); st != NVFP4_OK) return st;
   if (out == nullptr) return NVFP4_ERR_NULL;
   if (!aligned16(out) || ldo % (out_dtype == NVFP4_OUT_BF16 ? 8 : 4) != 0) return NVFP4_ERR_ALIGN;
-  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
   a.out_fp32 = out_dtype == NVFP4_OUT_FP32 ? 1 : 0;
   a.out = out;
   a.ldo = ldo;
+  if (nvfp4_status st = gemm_memory_ok(a); st != NVFP4_OK) return st;
   return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -239,7 +284,6 @@ nvfp4_status nvfp4_gemm_nvfp4_out(const uint8_t* a_codes, const uint8_t* a_scale
   if (nvfp4_status st = gemm_inputs_ok(a); st != NVFP4_OK) return st;
   if (out_tensor_scale == nullptr || out_codes == nullptr || out_scales == nullptr) return NVFP4_ERR_NULL;
   if (!aligned16(out_codes) || !aligned16(out_scales)) return NVFP4_ERR_ALIGN;
-  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
   a.out_fp32 = 0;
   a.out = nullptr;
   a.ldo = out_cols;
@@ -247,6 +291,7 @@ nvfp4_status nvfp4_gemm_nvfp4_out(const uint8_t* a_codes, const uint8_t* a_scale
   a.out_codes = out_codes;
   a.out_scales = out_scales;
   a.out_ts = out_tensor_scale;
+  if (nvfp4_status st = gemm_memory_ok(a); st != NVFP4_OK) return st;
   return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -261,6 +306,8 @@ nvfp4_status fp8_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, uint
       (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
     return NVFP4_ERR_ALIGN;
   if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  if (nvfp4_status st = check_pointers({x, codes, tensor_scale, tensor_scale_in, workspace}); st != NVFP4_OK)
+    return st;
   return from_cuda(nvfp4::launch_fp8_quantize(x, M, K, ldx, codes, static_cast<unsigned*>(workspace),
                                               tensor_scale_in, tensor_scale, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -275,6 +322,7 @@ nvfp4_status fp8_pack_weights(const void* w, int64_t K, int64_t N, int gated_int
       (reinterpret_cast<uintptr_t>(tensor_scale) & 3u) != 0)
     return NVFP4_ERR_ALIGN;
   if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  if (nvfp4_status st = check_pointers({w, codes, tensor_scale, workspace}); st != NVFP4_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   unsigned* amax = static_cast<unsigned*>(workspace);
   if (cudaMemsetAsync(amax, 0, nvfp4_workspace_bytes(), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
@@ -303,10 +351,10 @@ nvfp4_status fp8_gemm(const uint8_t* a_codes, const float* a_ts, const uint8_t* 
   if (nvfp4_status st = gemm_inputs_ok(a); st != NVFP4_OK) return st;
   if (out == nullptr) return NVFP4_ERR_NULL;
   if (!aligned16(out) || ldo % (out_dtype == NVFP4_OUT_BF16 ? 8 : 4) != 0) return NVFP4_ERR_ALIGN;
-  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
   a.out_fp32 = out_dtype == NVFP4_OUT_FP32 ? 1 : 0;
   a.out = out;
   a.ldo = ldo;
+  if (nvfp4_status st = gemm_memory_ok(a); st != NVFP4_OK) return st;
   return nvfp4::launch_gemm(a, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -326,6 +374,7 @@ nvfp4_status attention_fwd(const void* qkv, int64_t M, int64_t ld_qkv, int heads
   if (!aligned16(qkv) || !aligned16(workspace) || !aligned16(out) || ld_qkv % 8 != 0 || ldo % 8 != 0)
     return NVFP4_ERR_ALIGN;
   if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  if (nvfp4_status st = check_pointers({qkv, workspace, out, device_error}); st != NVFP4_OK) return st;
   return nvfp4::launch_attention(qkv, M, ld_qkv, heads, workspace, out, ldo, device_error,
                                  reinterpret_cast<cudaStream_t>(stream));
 }
@@ -346,6 +395,7 @@ nvfp4_status nvfp4_debug_wait_timeout(int* device_error, int64_t timeout_ns, nvf
   if (device_error == nullptr) return NVFP4_ERR_NULL;
   if (timeout_ns < 1 || timeout_ns > 10000000000ll) return NVFP4_ERR_ARG;
   if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  if (nvfp4_status st = check_pointers({device_error}); st != NVFP4_OK) return st;
   return from_cuda(nvfp4::launch_wait_timeout(device_error, static_cast<uint64_t>(timeout_ns),
                                               reinterpret_cast<cudaStream_t>(stream)));
 }

@@ -15,11 +15,11 @@
 // share weight tiles in L2.
 //   warp 0     (both CTAs) TMA producer of the codes: this CTA's A tile and its half of
 //              the B tile;
-//   warp 6     (both CTAs) TMA producer of the scales: this CTA's A scale tile and one of
-//              the two B scale bands, multicast to both CTAs (every CTA needs the scales of
-//              all 256 columns in its TMEM). Both producers' loads complete on the leader
-//              CTA's full barrier, where each of the leader's two producers announces its
-//              bytes for both CTAs;
+//   warp 6     (both CTAs) TMA producer of the scales: this CTA's A scale tile and both B
+//              scale bands (every CTA needs the scales of all 256 columns in its own TMEM).
+//              Both producers' loads complete on the leader CTA's full barrier, where each of
+//              the leader's two producers announces its bytes for both CTAs. Every load is a
+//              plain (non-multicast) TMA load into the issuing CTA's own shared memory;
 //   warp 1     (both CTAs) TMEM allocation (pair-collective); in the leader, the single
 //              MMA-issuing thread, whose commits release the stage and publish the
 //              accumulator in both CTAs;
@@ -374,10 +374,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_a, const CUtenso
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   // ---------------- TMA producers (both CTAs) ----------------
-  // warp 0: this CTA's A tile and its half of the B tile; warp 6:
-  // its A scale tile and one of the two B scale bands, multicast to both CTAs (every CTA
-  // needs the scales of all 256 columns). Both complete on the leader CTA's full barrier,
-  // on which each producer of the leader announces its bytes for both CTAs.
+  // warp 0: this CTA's A tile and its half of the B tile; warp 6: its A scale tile and both
+  // B scale bands (every CTA needs the scales of all 256 columns). Both complete on the
+  // leader CTA's full barrier, on which each producer of the leader announces its bytes for
+  // both CTAs.
   auto producer = [&](const bool codes_part) {
     const uint64_t pol = policy_evict_normal();
     uint32_t kc = 0;  // k-blocks issued so far (ring position)
@@ -402,8 +402,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_a, const CUtenso
           // scale tiles: row = band * k_atoms + first k-atom of the stage (4 atoms of 512 B)
           tma_load_2d_pair(sbase + kOffSfa + s * kSfaBytes, &tm_sfa, 0,
                            m_blk * k_atoms + kb * kKStepsPerStage, bar, pol);
-          tma_load_2d_pair_mc(sbase + kOffSfb + s * kSfbBytes + rank * (kSfbBytes / 2), &tm_sfb, 0,
-                              (n_blk * 2 + rank) * k_atoms + kb * kKStepsPerStage, bar, 0x3, pol);
+          // both 128-column B scale bands into this CTA's own shared memory (every CTA needs
+          // the scales of all 256 columns in its TMEM); plain loads, no multicast
+#pragma unroll
+          for (int h = 0; h < kBN / 128; ++h)
+            tma_load_2d_pair(sbase + kOffSfb + s * kSfbBytes + h * (kSfbBytes / 2), &tm_sfb, 0,
+                             (n_blk * 2 + h) * k_atoms + kb * kKStepsPerStage, bar, pol);
         }
         ++kc;
       }

@@ -1,13 +1,14 @@
 // nvfp4_quantize_noalloc: the activation quantizer for callers that cannot allocate device
-// memory (see include/nvfp4.h). Its scratch -- the word the tensor-amax pass reduces into
-// and a finished-CTA count -- lives in a fixed array inside this library instead of a
-// caller-provided workspace.
+// memory (see include/nvfp4.h). Its scratch -- the quantizer's 16 workspace bytes (the amax
+// word, two grid-barrier counters and a failure flag) -- lives in a fixed array inside this
+// library instead of a caller-provided workspace.
 
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "../../include/nvfp4.h"
+#include "nvfp4_internal.h"
 
 namespace {
 
@@ -49,20 +50,24 @@ extern "C" {
 
 nvfp4_status nvfp4_quantize_noalloc(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* codes,
                                     uint8_t* scales, float* tensor_scale, nvfp4_stream_t stream) {
-  if (M < 0 || K <= 0 || K % 64 != 0 || ldx < K) return NVFP4_ERR_SHAPE;
-  if (M == 0) return NVFP4_OK;
-  if (x == nullptr || codes == nullptr || scales == nullptr || tensor_scale == nullptr)
-    return NVFP4_ERR_NULL;
+  // Every check nvfp4_quantize makes (shapes, NULL, alignment, device, memory of the current
+  // device) comes first: a refused call touches neither the scratch nor the stream.
+  if (nvfp4_status st = nvfp4::check_quantize_args(x, M, K, ldx, codes, scales, tensor_scale, nullptr, nullptr,
+                                                   true);
+      st != NVFP4_OK || M == 0)
+    return st;
   // The quantizer's scratch must fit the fixed array; a larger need is refused, not truncated.
   if (nvfp4_workspace_bytes() > kNoAllocScratchBytes) return NVFP4_ERR_SHAPE;
   void* scratch = nullptr;
   if (nvfp4_status st = scratch_address(&scratch); st != NVFP4_OK) return st;
-  // Start from a zeroed scratch every call (the amax word and the finished-CTA count), so
-  // an earlier call that was interrupted cannot leave this shared array in a bad state.
-  if (cudaMemsetAsync(scratch, 0, nvfp4_workspace_bytes(), reinterpret_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
-    return NVFP4_ERR_LAUNCH;
-  return nvfp4_quantize(x, M, K, ldx, codes, scales, tensor_scale, nullptr, scratch, stream);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Start from a zeroed scratch every call, so an earlier call that was interrupted (or timed
+  // out) cannot leave this shared array in a bad state.
+  if (cudaMemsetAsync(scratch, 0, nvfp4_workspace_bytes(), s) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  return nvfp4::launch_quantize(x, M, K, ldx, codes, scales, static_cast<unsigned*>(scratch), nullptr,
+                                tensor_scale, s) == cudaSuccess
+             ? NVFP4_OK
+             : NVFP4_ERR_LAUNCH;
 }
 
 }  // extern "C"

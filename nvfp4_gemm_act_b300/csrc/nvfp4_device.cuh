@@ -98,27 +98,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
-// Same tile, multicast: written at offset `dst` of every CTA in `cta_mask` of the cluster,
-// each completing bytes on its own mbarrier at offset `bar`.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                               uint32_t bar, uint16_t cta_mask, uint64_t cache_hint) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(cache_hint)
-      : "memory");
-}
-
-// 1-D bulk copy, multicast to the CTAs in `cta_mask` (same offsets in each).
-__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                             uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -138,18 +117,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
       ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(cache_hint)
-      : "memory");
-}
-
-// Pair tile load, multicast: lands at offset `dst` in every CTA of `cta_mask`, and each
-// destination's bytes complete on the mbarrier at `bar`'s offset in that destination's pair
-// leader (`bar` is a leader's barrier, shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                                    uint32_t bar, uint16_t cta_mask, uint64_t cache_hint) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(cache_hint)
       : "memory");
 }
 
@@ -391,15 +358,6 @@ __device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mas
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// As tc_commit, arriving on the barrier at offset `bar` of every CTA in `cta_mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          bar),
-      "h"(cta_mask)
       : "memory");
 }
 

@@ -20,6 +20,13 @@ int sm_count();
 cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
                         unsigned* amax_bits, cudaStream_t s);
 
+// Host checks of nvfp4_quantize, in order: shapes (then M == 0 returns NVFP4_OK), NULL
+// pointers, alignment, the device, and that every pointer is memory of the current device.
+// `library_scratch`: the workspace is the library's own array (no NULL check on it).
+nvfp4_status check_quantize_args(const void* x, int64_t M, int64_t K, int64_t ldx, const uint8_t* codes,
+                                 const uint8_t* scales, const float* tensor_scale, const float* tensor_scale_in,
+                                 const void* workspace, bool library_scratch);
+
 // Quantize x [M, K] (row stride ldx). ts = *ts_in if ts_in, else amax/2688 of x: either one
 // cooperative single-pass launch (x fits in the SMs' shared memory) or amax_kernel reducing
 // into ws[0] and the quantize kernel reading it; both leave ws[0..3] zeroed again.

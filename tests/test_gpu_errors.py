@@ -33,3 +33,32 @@ def test_host_checks_raise_before_launch():
     with pytest.raises(nv.Nvfp4Error) as e:
         nv.nvfp4_quantize(x)
     assert e.value.status == 2
+
+
+def test_host_memory_is_refused_before_launch():
+    # Pinned host memory is reachable from the GPU through unified addressing, so a kernel
+    # given its address would silently read host memory; the C ABI refuses any pointer that
+    # is not memory of the current device (NVFP4_ERR_ARG) before launching anything. The
+    # pointers chosen are ones that kernels only ever read with plain loads.
+    dev = "cuda:0"
+    L = nv.lib()
+    x_host = torch.zeros((128, 256), dtype=torch.bfloat16).pin_memory()
+    qa = nv._alloc_nvfp4(128, 256, dev)
+    ts_in = torch.ones(1, dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream().cuda_stream
+    st = L.nvfp4_quantize(x_host.data_ptr(), 128, 256, 256, qa.codes.data_ptr(), qa.scales.data_ptr(),
+                          qa.ts.data_ptr(), ts_in.data_ptr(), None, s)
+    assert st == 7  # NVFP4_ERR_ARG
+    # the same call with device memory runs
+    x_dev = x_host.to(dev)
+    assert L.nvfp4_quantize(x_dev.data_ptr(), 128, 256, 256, qa.codes.data_ptr(), qa.scales.data_ptr(),
+                            qa.ts.data_ptr(), ts_in.data_ptr(), None, s) == 0
+    # a GEMM whose bias lives in pinned host memory is refused too
+    qb = nv.nvfp4_pack_weights(torch.zeros((256, 256), dtype=torch.bfloat16, device=dev))
+    bias_host = torch.zeros(256, dtype=torch.float32).pin_memory()
+    out = torch.empty((128, 256), dtype=torch.bfloat16, device=dev)
+    st = L.nvfp4_gemm(qa.codes.data_ptr(), qa.scales.data_ptr(), qa.ts.data_ptr(), qb.codes.data_ptr(),
+                      qb.scales.data_ptr(), qb.ts.data_ptr(), 128, 256, 256, 0, bias_host.data_ptr(), None, 256, 0,
+                      1e-6, 0, out.data_ptr(), 256, None, s)
+    assert st == 7
+    torch.cuda.synchronize()
