@@ -361,9 +361,10 @@ def gemm_block_form_ref(a_codes, a_scales, a_ts, b_codes, b_scales, b_ts):
 # ----------------------------------------------------------------------------------------
 
 def round_to_bf16(y: np.ndarray) -> np.ndarray:
-    """fp64 -> nearest bf16 value (8 significant bits, ties to even), returned as fp64."""
+    """fp64 -> nearest bf16 value (8 significant bits, ties to even), returned as fp64. A zero
+    keeps its sign (IEEE rounding: -0 rounds to -0, as a tiny negative value does)."""
     y = np.asarray(y, np.float64)
-    out = np.zeros_like(y)
+    out = np.where(y == 0, y, 0.0)
     nz = (y != 0) & np.isfinite(y)
     _, e = np.frexp(y[nz])                      # |y| = m * 2**e, m in [0.5, 1)
     quantum = np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
@@ -473,14 +474,15 @@ def attention_ref(q, k, v) -> np.ndarray:
 
 
 def _linear_ref(x, w, bias, epilogue, quantized, gamma=None, head_dim=256, norm_cols=0, eps=1e-6,
-                tensor_scale=None):
+                tensor_scale=None, packed=None):
     """One linear layer of the block: quantized, the layer as the NVFP4 path defines it (x and
     W quantized with their own amax scales unless ``tensor_scale`` fixes x's; fp64 GEMM and
-    epilogue); not quantized, the exact fp64 layer epilogue(x @ W + bias)."""
+    epilogue); not quantized, the exact fp64 layer epilogue(x @ W + bias). ``packed``: W
+    already passed through pack_weights_ref (with the layer's interleave), to skip repacking."""
     kw = dict(bias=bias, gamma=gamma, head_dim=head_dim, norm_cols=norm_cols, eps=eps)
     if quantized:
         a = quantize_ref(x, tensor_scale)
-        b = pack_weights_ref(w, gated_interleave=(epilogue == EPI_GATED_SILU))
+        b = packed if packed is not None else pack_weights_ref(w, gated_interleave=(epilogue == EPI_GATED_SILU))
         return gemm_ref(*a, *b, epilogue, **kw)
     c = np.asarray(x, np.float64) @ np.asarray(w, np.float64)
     if bias is not None:
@@ -493,7 +495,7 @@ def _linear_ref(x, w, bias, epilogue, quantized, gamma=None, head_dim=256, norm_
 
 
 def dit_block_ref(x, layers, heads: int, head_dim: int, eps: float = 1e-6, ts_mid=None,
-                  quantized: bool = True, rows=None):
+                  quantized: bool = True, rows=None, packed=None):
     """One DiT block's linears with attention between the first two, in the order of the page
     "How fal made Ideogram V4 6x faster" (each large GEMM followed by its small op, fused).
 
@@ -515,26 +517,29 @@ def dit_block_ref(x, layers, heads: int, head_dim: int, eps: float = 1e-6, ts_mi
     only; every token's K and V still enter the attention, and the dynamic scales of the
     quantized block's activations are still those of all tokens, so the stages that feed a
     dynamic scale run over all tokens and the last two layers over ``rows`` (the default
-    ts_mid is then amax / 2688 over those rows). Returns (y, dict of the intermediates, for
-    all tokens or for ``rows`` where a stage ran only there, and ts_mid).
+    ts_mid is then amax / 2688 over those rows). ``packed``: the four weights already passed
+    through pack_weights_ref (the up-projection's with the gated interleave), to skip
+    repacking them. Returns (y, dict of the intermediates, for all tokens or for ``rows``
+    where a stage ran only there, and ts_mid).
     """
+    pk = packed if packed is not None else (None, None, None, None)
     hidden = heads * head_dim
     rnd = round_to_bf16 if quantized else (lambda z: np.asarray(z, np.float64))
     (w1, b1, g1), (w2, b2, _), (w3, b3, _), (w4, b4, _) = layers
     M = x.shape[0]
     t = rnd(_linear_ref(x, w1, b1, EPI_HEAD_RMSNORM, quantized, gamma=g1, head_dim=head_dim,
-                        norm_cols=2 * hidden, eps=eps))
+                        norm_cols=2 * hidden, eps=eps, packed=pk[0]))
     qkv = t.reshape(M, 3, heads, head_dim).transpose(1, 2, 0, 3)    # [3, heads, M, head_dim]
     q_rows = qkv[0] if (rows is None or quantized) else qkv[0][:, rows]
     a = rnd(attention_ref(q_rows, qkv[1], qkv[2]).transpose(1, 0, 2).reshape(-1, hidden))
-    o = rnd(_linear_ref(a, w2, b2, EPI_BIAS, quantized))
+    o = rnd(_linear_ref(a, w2, b2, EPI_BIAS, quantized, packed=pk[1]))
     o_ts = tensor_scale_ref(o) if quantized else None
     if rows is not None and quantized:
         o_in = o[rows]
     else:
         o_in = o
-    u = rnd(_linear_ref(o_in, w3, b3, EPI_GATED_SILU, quantized, tensor_scale=o_ts))
+    u = rnd(_linear_ref(o_in, w3, b3, EPI_GATED_SILU, quantized, tensor_scale=o_ts, packed=pk[2]))
     if quantized and ts_mid is None:
         ts_mid = tensor_scale_ref(u)
-    y = rnd(_linear_ref(u, w4, b4, EPI_BIAS, quantized, tensor_scale=ts_mid))
+    y = rnd(_linear_ref(u, w4, b4, EPI_BIAS, quantized, tensor_scale=ts_mid, packed=pk[3]))
     return y, {"qkv": t, "attention": a, "out_proj": o, "up": u, "ts_mid": ts_mid}

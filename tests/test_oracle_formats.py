@@ -112,6 +112,15 @@ def test_round_to_bf16_hand():
 def test_round_to_bf16_matches_torch_on_fp32_values():
     torch = pytest.importorskip("torch")
     v = np.random.default_rng(3).standard_normal(50000).astype(np.float32) * 10
+    # signed zeros and values that round to a signed zero or the smallest subnormals
+    v = np.concatenate([v, np.array([0.0, -0.0, 1e-45, -1e-45, 2e-41, -2e-41, 1e-40, -1e-40], np.float32)])
     ours = R.round_to_bf16(v.astype(np.float64))
     theirs = torch.from_numpy(v).to(torch.bfloat16).double().numpy()
     assert np.array_equal(ours, theirs)
+    assert np.array_equal(np.signbit(ours), np.signbit(theirs))  # the sign of zero too
+
+
+def test_round_to_bf16_keeps_the_sign_of_zero():
+    # IEEE round to nearest: -0 stays -0 (the quantizer codes it 0x8, +0 as 0x0)
+    out = R.round_to_bf16(np.array([-0.0, 0.0]))
+    assert list(np.signbit(out)) == [True, False] and np.all(out == 0.0)
