@@ -34,6 +34,22 @@ UNIT = "TFLOP/s"
 NOMINAL_FP4_PF = 15.0          # B300 dense FP4 (NVIDIA's Blackwell Ultra figure)
 FP4_OVER_BF16 = 13.5 / 2.25    # nominal dense FP4 : BF16 ratio used to scale the measured peak
 FLUSH_BYTES = 256 << 20        # > 126 MB L2
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: a 256 MiB write (every line of the step's inputs and
+    outputs is evicted), then a read of a second 256 MiB buffer, which writes those dirty flush
+    lines back to HBM outside the timed region and leaves L2 holding clean lines only, so no
+    step pays for write-back traffic that is not its own."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
 WORKLOAD_NAME = ("dit_block_linears_m4608: qkv+head_rmsnorm [4608x3072x9216], "
                  "up+gated_silu [4608x3072x24576], down+bias [4608x12288x3072], "
                  "each with its bf16->nvfp4 activation quantize")
@@ -64,6 +80,10 @@ def parse_args(argv=None):
                    help="one DiT block's linears chained at 4608 tokens: per-stage CUDA-event times")
     p.add_argument("--sweep", action="store_true",
                    help="batch sweep: one JSON line per (M, GEMM), M in 512..18432")
+    p.add_argument("--mma-ceiling", action="store_true",
+                   help="tensor-pipe rate of tcgen05.mma (NVFP4 / FP8 / BF16 kinds, cta_group 1/2, N 64..256): "
+                        "cycles per instruction on one SM and on all SMs")
+    p.add_argument("--probe-iters", type=int, default=20000)
     return p.parse_args(argv)
 
 
@@ -291,7 +311,7 @@ def run_ours(args, world, rank, local):
     layers = [Layer(w, dev) for w in (W.QKV_RMSNORM, W.GATED_UP, W.DOWN_BIAS)
               if args.only is None or w.name == args.only]
     flops_step = sum(l.w.flops for l in layers)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     ops = []  # (name, callable, flops, algorithmic bytes)
     for l in layers:
         w = l.w
@@ -334,7 +354,7 @@ def run_ours(args, world, rank, local):
         nvml_index = local
     # pass 1 (eager, an event before every launch): the per-kernel breakdown and the roofline
     for k in range(K):
-        flush.zero_()              # evict L2 between steps (outside the timed events)
+        flush()                    # evict L2 between steps (outside the timed events)
         step(events[k])
     torch.cuda.synchronize()
     per_op = np.array([[events[k][i].elapsed_time(events[k][i + 1]) for i in range(len(ops))]
@@ -351,14 +371,14 @@ def run_ours(args, world, rank, local):
     with torch.cuda.graph(graph):
         step()
     for _ in range(max(args.warmup, 3)):
-        flush.zero_()
+        flush()
         graph.replay()
     gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(nvml_index) as clocks:
         for k in range(K):
-            flush.zero_()              # evict L2 between steps (outside the timed events)
+            flush()                    # evict L2 between steps (outside the timed events)
             gev[k][0].record()
             graph.replay()
             gev[k][1].record()
@@ -390,6 +410,28 @@ def run_ours(args, world, rank, local):
         breakdown[name] = e
     gemm_ms = sum(mean_op[i] for i, o in enumerate(ops) if o[2])
     traffic = read_traffic(dom_name)
+    # the down-projection input's quantizer with a static tensor scale (one streaming pass; the
+    # step uses the dynamic scale: amax pass + quantize pass), timed alone, L2 flushed first
+    down = [l for l in layers if l.w.name == "down_bias"]
+    if down:
+        l = down[0]
+        ts_static = nv.nvfp4_quantize(l.x).ts.clone()  # the dynamic scale of this X, reused as a static one
+        st_ms = []
+        for it in range(max(args.warmup, 3) + K):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            nv.nvfp4_quantize(l.x, tensor_scale_in=ts_static, out=l.qa)
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= max(args.warmup, 3):
+                st_ms.append(e0.elapsed_time(e1))
+        ms = float(np.median(st_ms))
+        by = ops[[o[0] for o in ops].index("quantize_down_bias")][3]
+        breakdown["quantize_down_bias_static_scale"] = {
+            "ms": round(ms, 5), "gbs": round(by / (ms / 1e3) / 1e9, 1),
+            "frac_of_hbm_measured": round(by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "note": "not part of the step: the same X with a static tensor scale (one pass), median of K"}
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -398,7 +440,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME if args.only is None else f"{args.only} only (profiling)",
                    "M": 4608, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "l2": "flushed between steps, outside the timed events: 256 MiB write, then a 256 MiB read of another buffer (L2 left holding clean lines)",
                    "timing": "each step replayed as one CUDA graph (events around the replay); the per-kernel breakdown and the roofline from an eager pass with an event before every launch",
                    "weights": "packed offline, resident in HBM",
                    "flops_per_step": flops_step},
@@ -529,19 +571,68 @@ def _oracle_layers():
     return [OracleLayer(w) for w in (W.QKV_RMSNORM, W.GATED_UP, W.DOWN_BIAS)]
 
 
+def _cpu_cases(rows_per_gemm: int):
+    """(config label, workload, sampled rows) for every config: C1 whole; C2-C4 on
+    ``rows_per_gemm`` rows spread over M; the C5 batch sweep once per batch size: QKV at 512
+    and 4608, down at 1024 and 9216, up (the costliest weight to dequantize) at 18432, so that
+    every size and every GEMM is timed while the oracle's whole-weight dequantization, which
+    does not depend on M, is not repeated fifteen times."""
+    from nvfp4_gemm_act_b300 import workloads as W
+    cases = [("C1", W.TINY_BIAS, np.arange(W.TINY_BIAS.M))]
+    for label, w in (("C2", W.QKV_RMSNORM), ("C3", W.GATED_UP), ("C4", W.DOWN_BIAS)):
+        cases.append((label, w, np.arange(rows_per_gemm) * (w.M // rows_per_gemm)))
+    pick = {512: "qkv_rmsnorm", 1024: "down_bias", 4608: "qkv_rmsnorm", 9216: "down_bias", 18432: "gated_up"}
+    for w in W.sweep_workloads():
+        if w.name == f"{pick[w.M]}_m{w.M}":
+            cases.append(("C5", w, np.arange(rows_per_gemm) * (w.M // rows_per_gemm)))
+    return cases
+
+
 def cpu_baseline(rows_per_gemm: int):
-    layers = _oracle_layers()
-    rows = np.arange(rows_per_gemm) * (4608 // rows_per_gemm)
-    t0 = time.perf_counter()
-    for l in layers:
-        l.run(rows)
-    el = time.perf_counter() - t0
-    flops = sum(2 * len(rows) * l.w.N * l.w.K for l in layers)
-    return {"value": round(flops / el / 1e12, 6), "unit": UNIT, "cores": cpu_threads(),
+    """The oracle, as it stands, on the host cores: for each config, the quantize stage (the
+    tensor amax over the whole X, then the block quantizer on the sampled rows) and the GEMM +
+    epilogue stage (dequantize, fp64 matmul, epilogue) timed separately. Inputs are generated
+    and the weights packed by the oracle before the clock starts (packing is offline in the
+    method). ``value`` = the sampled GEMM FLOPs over both stages' total time."""
+    from nvfp4_gemm_act_b300 import workloads as W
+    from oracle import nvfp4_ref as R
+    packed = {}
+    per_config = {}
+    flops = 0
+    total_s = 0.0
+    wall0 = time.perf_counter()
+    for label, w, rows in _cpu_cases(rows_per_gemm):
+        base = w.name.rsplit("_m", 1)[0]
+        if base not in packed:
+            packed[base] = R.pack_weights_ref(W.make_w(w).float().numpy(), w.epilogue == W.EPI_GATED_SILU)
+        x = W.make_x(w).float().numpy()
+        bias, gamma = W.make_bias(w), W.make_gamma(w)
+        bias = None if bias is None else bias.double().numpy()
+        gamma = None if gamma is None else gamma.double().numpy()
+        t0 = time.perf_counter()
+        a = R.quantize_ref(x[rows], R.tensor_scale_ref(x))
+        t1 = time.perf_counter()
+        R.gemm_ref(*a, *packed[base], w.epilogue, bias=bias, gamma=gamma, head_dim=w.head_dim,
+                   norm_cols=w.norm_cols, eps=w.eps)
+        t2 = time.perf_counter()
+        del x
+        f = 2 * len(rows) * w.N * w.K
+        flops += f
+        total_s += t2 - t0
+        per_config[f"{label} {w.name}"] = {
+            "M": w.M, "N": w.N, "K": w.K, "rows": int(len(rows)),
+            "quantize_s": round(t1 - t0, 4),
+            "quantize_gbs": round((w.M * w.K * 2 + len(rows) * w.K * 2.5625) / (t1 - t0) / 1e9, 3),
+            "gemm_s": round(t2 - t1, 4), "gemm_tflops": round(f / (t2 - t1) / 1e12, 7)}
+    return {"value": round(flops / total_s / 1e12, 7), "unit": UNIT, "cores": cpu_threads(),
             "kind": "oracle",
-            "sample": f"{len(rows)} rows of each of the 3 GEMMs (quantize incl. full-X amax, "
-                      f"dequantize, fp64 matmul, epilogue); weights packed by the oracle "
-                      f"before timing; {el:.1f} s"}
+            "sample": (f"C1 whole; C2-C4, and the C5 sweep once per M (QKV at 512/4608, down at "
+                       f"1024/9216, up at 18432), on "
+                       f"{rows_per_gemm} rows spread over M. Quantize (full-X amax + block quantizer on the rows) and GEMM + "
+                       f"epilogue (dequantize, fp64 matmul, epilogue) timed separately; inputs generated "
+                       f"and weights packed by the oracle before timing; {total_s:.1f} s timed, "
+                       f"{time.perf_counter() - wall0:.0f} s with set-up"),
+            "per_config": per_config}
 
 
 def run_reference(args, world, rank):
@@ -590,7 +681,7 @@ def run_sweep(args):
     dev = "cuda:0"
     peaks, _ = measured_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     packed = {}
     for w in W.sweep_workloads():
         base = w.name.rsplit("_m", 1)[0]
@@ -608,7 +699,7 @@ def run_sweep(args):
         times = {"quantize": [], "gemm": []}
         for it in range(max(args.warmup, 3) + args.steps):
             for name, fn in (("quantize", l.quantize), ("gemm", l.gemm)):
-                flush.zero_()
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 fn()
@@ -645,11 +736,11 @@ def run_chain(args):
     qb_dn = nv.nvfp4_pack_weights(W.make_w(down).to(dev))
     bias_dn = W.make_bias(down).to(dev)
     y_mid = nv.nvfp4_gemm(qa, qb_up, up.epilogue)
-    ts_mid = (y_mid.float().abs().max() / 2688.0).reshape(1).contiguous()
+    ts_mid = nv.nvfp4_quantize(y_mid).ts  # the library's dynamic tensor scale of the bf16 output
     q_mid = nv._alloc_nvfp4(up.M, up.out_cols, dev)
     ws = torch.zeros(16, dtype=torch.uint8, device=dev)
     out = torch.empty((down.M, down.out_cols), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def fused():
         m = nv.nvfp4_gemm_nvfp4_out(qa, qb_up, up.epilogue, ts_mid, out=q_mid)
@@ -666,7 +757,7 @@ def run_chain(args):
     for name, fn in variants.items():
         ts = []
         for it in range(max(args.warmup, 3) + args.steps):
-            flush.zero_()
+            flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -694,7 +785,7 @@ def run_fp8(args):
     dev = "cuda:0"
     peaks, _ = measured_peaks()
     fp8_peak = peaks["bf16_tflops"] * 2.0
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     spun = False
     for w in (W.QKV_RMSNORM, W.GATED_UP, W.DOWN_BIAS):
         if args.only is not None and w.name != args.only:
@@ -726,7 +817,7 @@ def run_fp8(args):
         with sampler:
             for it in range(args.steps):
                 for name, fn in ops.items():
-                    flush.zero_()
+                    flush()
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record()
                     fn()
@@ -761,7 +852,7 @@ def run_attention(args):
     out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     q, k, v = qkv.view(M, 3, heads, hd).permute(1, 2, 0, 3).unsqueeze(1).unbind(0)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     impls = {"kernel": lambda: nv.attention(qkv, heads, out=out, workspace=ws, device_error=err),
              "torch_default": lambda: F.scaled_dot_product_attention(q, k, v)}
     try:
@@ -787,7 +878,7 @@ def run_attention(args):
         ts = []
         with sampler if name == "kernel" else _nullctx():
             for _ in range(args.steps):
-                flush.zero_()
+                flush()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 fn()
@@ -825,13 +916,13 @@ def run_dit_block(args):
     M = 4608
     blk, x = seeded_dit_block(M, dev, attention_impl=args.attention_impl)
     blk.calibrate(x)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     times = {}
     total = []
     sampler = ClockSampler(0)
 
     def one(t):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         y = blk(x, timings=t)
@@ -853,7 +944,7 @@ def run_dit_block(args):
     replay, _ = blk.graph(x)
     graph_ms = []
     for it in range(max(args.warmup, 3) + args.steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         replay()
@@ -877,6 +968,46 @@ def run_dit_block(args):
                       "clocks": sampler.summary()}), flush=True)
 
 
+def run_mma_ceiling(args):
+    """The tensor pipe's instruction rate (nvfp4_debug_mma_rate): for each kind, cta_group and N,
+    `--probe-iters` back-to-back instructions per CTA (pair) on one SM (pair) and on every SM;
+    one JSON line each with the median cycles per instruction, FLOP per cycle per SM, and the
+    whole-GPU rate from the per-CTA nanoseconds (sum of FLOPs over the slowest CTA's time)."""
+    import torch
+
+    import nvfp4_gemm_act_b300 as nv
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    iters = args.probe_iters
+    nv.nvfp4_debug_mma_rate("nvfp4", 2, 256, iters, sms // 2, device_error=err)  # warm-up, clocks settle
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    with sampler:
+        for kind in ("nvfp4", "fp8", "bf16"):
+            for cg in (1, 2):
+                for n in (64, 128, 256):
+                    for ctas in (1, sms // cg):
+                        nv.nvfp4_debug_mma_rate(kind, cg, n, iters, ctas, device_error=err)  # warm
+                        r = nv.nvfp4_debug_mma_rate(kind, cg, n, iters, ctas, device_error=err)
+                        torch.cuda.synchronize()
+                        r = r.cpu().numpy()
+                        assert (r > 0).all(), f"probe wait ran out: {kind} cta_group {cg} n {n}"
+                        cyc = float(np.median(r[:, 0])) / iters
+                        m = 128 * cg
+                        flop = 2 * m * n * nv.PROBE_K[kind]
+                        print(json.dumps({
+                            "mma_ceiling": kind, "cta_group": cg, "M": m, "N": n, "K": nv.PROBE_K[kind],
+                            "ctas": ctas, "sms": ctas * cg, "iters": iters,
+                            "cycles_per_instr": round(cyc, 2),
+                            "flop_per_clk_per_sm": round(flop / cyc / cg, 1),
+                            "tflops_all_ctas": round(flop * iters * ctas / (float(r[:, 1].max()) * 1e-9) / 1e12, 1),
+                            "sm_mhz_implied": round(float(np.median(r[:, 0] / r[:, 1])) * 1e3, 0)}), flush=True)
+    assert nv.nvfp4_get_device_error(err) == 0
+    print(json.dumps({"mma_ceiling_clocks": sampler.summary()}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
@@ -894,6 +1025,9 @@ def main(argv=None):
         return
     if args.sweep:
         run_sweep(args)
+        return
+    if args.mma_ceiling:
+        run_mma_ceiling(args)
         return
     if args.impl == "reference":
         run_reference(args, world, rank)

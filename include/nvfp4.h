@@ -312,6 +312,33 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status status);
 NVFP4_API nvfp4_status nvfp4_debug_wait_timeout(int *device_error, int64_t timeout_ns,
                                       nvfp4_stream_t stream);
 
+/* Instruction kinds of nvfp4_debug_mma_rate. */
+typedef enum nvfp4_probe_kind {
+  NVFP4_PROBE_NVFP4 = 0,  /* tcgen05.mma kind::mxf4nvf4.block_scale.block16, K = 64 */
+  NVFP4_PROBE_FP8 = 1,    /* tcgen05.mma kind::f8f6f4 (E4M3 x E4M3), K = 32 */
+  NVFP4_PROBE_BF16 = 2    /* tcgen05.mma kind::f16 (BF16 x BF16), K = 16 */
+} nvfp4_probe_kind;
+
+/*
+ * nvfp4_debug_mma_rate -- measures the rate at which this device's tensor pipe retires one
+ * tcgen05.mma instruction kind and shape, the ceiling of any GEMM built from it (the fused
+ * GEMM above issues NVFP4 at cta_group 2, N = 256).
+ * Launches `ctas` CTAs (cta_group 1: M = 128 on one SM each) or `ctas` CTA pairs (cta_group
+ * 2: M = 256 across two SMs), one per SM; one thread of each (of each pair's leader) issues
+ * `iters` back-to-back instructions on zero operands held in shared memory (128-byte
+ * swizzled, K-major, 32 bytes of each row per instruction; NVFP4 block scales in TMEM) into
+ * a TMEM accumulator. It computes nothing useful.
+ *   out  device int64 [2 * ctas], zero-filled by the caller: out[2c] = SM cycles and
+ *        out[2c + 1] = nanoseconds from the first issue to the completion of the last
+ *        instruction, for CTA (pair) c; -1 if a device wait ran out.
+ * FLOP per instruction: 2 * M * n * K.
+ * Rules: kind one of nvfp4_probe_kind; cta_group 1 or 2; n in {64, 128, 192, 256};
+ * 1 <= iters <= 4,000,000; 1 <= ctas <= SM count (cta_group 1) or SM count / 2 (cta_group 2).
+ */
+NVFP4_API nvfp4_status nvfp4_debug_mma_rate(nvfp4_probe_kind kind, int cta_group, int n, int64_t iters,
+                                            int ctas, int64_t *out, int *device_error,
+                                            nvfp4_stream_t stream);
+
 /*
  * nvfp4_quantize_noalloc -- nvfp4_quantize (dynamic tensor scale) without a workspace
  * argument, for callers that cannot allocate device memory. The pages have no counterpart:

@@ -43,6 +43,8 @@ _SIGS = {
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "nvfp4_debug_mma_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, ctypes.c_int, _P,
+                                            _P, _P]),
     "fp8_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "fp8_pack_weights": (ctypes.c_int, [_P, _I64, _I64, ctypes.c_int, _P, _P, _P, _P]),
     "fp8_gemm": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P, ctypes.c_int, _I64,
@@ -300,4 +302,19 @@ def nvfp4_quantize_noalloc(x: torch.Tensor, out: Optional[Nvfp4Tensor] = None,
     _check("nvfp4_quantize_noalloc", lib().nvfp4_quantize_noalloc(
         _ptr(x), M, K, x.stride(0), _ptr(out.codes), _ptr(out.scales), _ptr(out.ts),
         _stream(stream)))
+    return out
+
+
+PROBE_KINDS = {"nvfp4": 0, "fp8": 1, "bf16": 2}
+PROBE_K = {"nvfp4": 64, "fp8": 32, "bf16": 16}
+
+
+def nvfp4_debug_mma_rate(kind: str, cta_group: int, n: int, iters: int, ctas: int,
+                         device_error: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Tensor-pipe rate probe: int64 [ctas, 2] of (SM cycles, ns) for `iters` back-to-back
+    tcgen05.mma of `kind` ("nvfp4", "fp8", "bf16") at M = 128 * cta_group, N = n, per CTA (pair).
+    Asynchronous on the stream; read the result after synchronizing."""
+    out = torch.zeros((ctas, 2), dtype=torch.int64, device=torch.cuda.current_device())
+    _check("nvfp4_debug_mma_rate", lib().nvfp4_debug_mma_rate(
+        PROBE_KINDS[kind], cta_group, n, iters, ctas, _ptr(out), _ptr(device_error), _stream(stream)))
     return out

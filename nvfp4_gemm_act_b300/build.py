@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libnvfp4.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "attention.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "attention.cu", "noalloc.cu", "mma_probe.cu"]
 HEADERS = ["nvfp4_device.cuh", "nvfp4_internal.h", "pointer_check.h"]
 
 NVCC_FLAGS = [

@@ -400,4 +400,20 @@ nvfp4_status nvfp4_debug_wait_timeout(int* device_error, int64_t timeout_ns, nvf
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+nvfp4_status nvfp4_debug_mma_rate(nvfp4_probe_kind kind, int cta_group, int n, int64_t iters, int ctas,
+                                  int64_t* out, int* device_error, nvfp4_stream_t stream) {
+  if (kind != NVFP4_PROBE_NVFP4 && kind != NVFP4_PROBE_FP8 && kind != NVFP4_PROBE_BF16) return NVFP4_ERR_ARG;
+  if (cta_group != 1 && cta_group != 2) return NVFP4_ERR_ARG;
+  if (n != 64 && n != 128 && n != 192 && n != 256) return NVFP4_ERR_SHAPE;
+  if (iters < 1 || iters > 4000000) return NVFP4_ERR_ARG;
+  if (out == nullptr) return NVFP4_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(out) & 7u) != 0) return NVFP4_ERR_ALIGN;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  if (ctas < 1 || ctas > nvfp4::sm_count() / cta_group) return NVFP4_ERR_SHAPE;
+  if (nvfp4_status st = check_pointers({out, device_error}); st != NVFP4_OK) return st;
+  return nvfp4::launch_mma_probe(static_cast<int>(kind), cta_group, n, static_cast<int>(iters), ctas,
+                                 reinterpret_cast<long long*>(out), device_error,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

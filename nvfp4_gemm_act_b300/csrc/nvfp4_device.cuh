@@ -437,13 +437,41 @@ constexpr float kFltMin = 1.17549435082e-38f;  // 2^-126
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// 8 bf16 values (in memory order) -> 4 bytes of E2M1 codes, element 2j in the low nibble.
+// Two fp32 values as one packed pair (lo in the low half) and the packed product of two pairs:
+// each half rounded to nearest even exactly as a scalar fp32 multiply.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t p;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(p) : "f"(lo), "f"(hi));
+  return p;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Four packed pairs -> four bytes of E2M1 codes (nearest even, saturating), byte j from pair
+// j, its low nibble from the pair's low half.
+__device__ __forceinline__ uint32_t e2m1x8(uint64_t p0, uint64_t p1, uint64_t p2, uint64_t p3) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .f32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      "mov.b64 {l0, h0}, %1;\n\tmov.b64 {l1, h1}, %2;\n\tmov.b64 {l2, h2}, %3;\n\tmov.b64 {l3, h3}, %4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, h0, l0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, h1, l1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, h2, l2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, h3, l3;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "l"(p0), "l"(p1), "l"(p2), "l"(p3));
+  return r;
+}
+
+// 8 bf16 values (in memory order) -> 4 bytes of E2M1 codes, element 2j in the low nibble:
+// code = E2M1(fp32(x * inv)), the four products of each pair of words in packed multiplies.
 __device__ __forceinline__ uint32_t encode8(const uint4& v, float inv) {
-  const uint32_t b0 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.x), inv), __fmul_rn(bf16_hi(v.x), inv));
-  const uint32_t b1 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.y), inv), __fmul_rn(bf16_hi(v.y), inv));
-  const uint32_t b2 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.z), inv), __fmul_rn(bf16_hi(v.z), inv));
-  const uint32_t b3 = cvt_e2m1x2(__fmul_rn(bf16_lo(v.w), inv), __fmul_rn(bf16_hi(v.w), inv));
-  return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  const uint64_t iv = f32x2(inv, inv);
+  return e2m1x8(mul_f32x2(f32x2(bf16_lo(v.x), bf16_hi(v.x)), iv), mul_f32x2(f32x2(bf16_lo(v.y), bf16_hi(v.y)), iv),
+                mul_f32x2(f32x2(bf16_lo(v.z), bf16_hi(v.z)), iv), mul_f32x2(f32x2(bf16_lo(v.w), bf16_hi(v.w)), iv));
 }
 
 // max(|a|, |b|) per bf16 lane (the sign of the result is discarded by the caller).
@@ -492,10 +520,17 @@ __device__ __forceinline__ uint32_t quantize_block(const uint4& lo, const uint4&
   const float bamax = absmax16(lo, hi);
   uint32_t s;
   if (sr.fast) {
+    // both ends of the window in one packed multiply and one paired conversion (codes of
+    // non-negative values: bits 0-7 from the low end, 8-15 from the high end)
     const float qa = __fmul_rn(bamax, sr.rcp_six_ts);
-    const uint32_t s_lo = cvt_e4m3(__fmul_rn(qa, 1.0f - 0x1p-20f));
-    const uint32_t s_hi = cvt_e4m3(__fmul_rn(qa, 1.0f + 0x1p-20f));
-    s = s_lo == s_hi ? s_lo : cvt_e4m3(__fdiv_rn(bamax, sr.six_ts));
+    uint32_t ends;
+    {
+      float e_lo, e_hi;
+      const uint64_t e = mul_f32x2(f32x2(qa, qa), f32x2(1.0f - 0x1p-20f, 1.0f + 0x1p-20f));
+      asm("mov.b64 {%0, %1}, %2;" : "=f"(e_lo), "=f"(e_hi) : "l"(e));
+      ends = cvt_e4m3x2(e_lo, e_hi);
+    }
+    s = (ends & 0xFFu) == (ends >> 8) ? (ends & 0xFFu) : cvt_e4m3(__fdiv_rn(bamax, sr.six_ts));
   } else {
     s = cvt_e4m3(__fdiv_rn(bamax, sr.six_ts));
   }

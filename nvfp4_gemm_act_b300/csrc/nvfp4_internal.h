@@ -89,4 +89,8 @@ nvfp4_status launch_attention(const void* qkv, int64_t M, int64_t ld_qkv, int he
 
 cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t s);
 
+// Validated arguments of nvfp4_debug_mma_rate in, the probe kernel launched.
+nvfp4_status launch_mma_probe(int kind, int cta_group, int n, int iters, int ctas, long long* out, int* err,
+                              cudaStream_t s);
+
 }  // namespace nvfp4

@@ -219,12 +219,13 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
 
 // ---------------------------------------------------------------------------------------
 // Single-pass quantizer for activations that fit in the shared memory of the whole GPU (a
-// dynamic tensor scale only): one cooperative launch, one CTA per SM. CTA b bulk-copies
-// rows [b R, b R + R) of x into its shared memory (one copy and one mbarrier per row),
-// reduces their amax while the rows land, and joins a grid-wide barrier on workspace words
-// (bounded spin; the cooperative launch guarantees every CTA is resident). It then reads the
-// tensor amax and quantizes its rows from shared memory: x is read from HBM once, in one
-// launch, instead of twice in two.
+// dynamic tensor scale only): one cooperative launch, one CTA per SM. CTA b loads rows
+// [b R, b R + R) of x into its shared memory -- all 1024 threads, 16-byte loads in batches of
+// six, so each SM keeps ~100 KB of x in flight (bulk copies from HBM keep far fewer bytes in
+// flight per SM) -- taking the amax from the registers on the way, and joins a grid-wide
+// barrier on workspace words (bounded spin; the cooperative launch guarantees every CTA is
+// resident). It then reads the tensor amax and quantizes its rows from shared memory: x is
+// read from HBM once, in one launch, instead of twice in two.
 //
 // Workspace words: ws[0] amax bits (atomic max), ws[1] CTAs arrived, ws[2] CTAs departed,
 // ws[3] failure flag. The CTA that departs last has seen every CTA pass the barrier and zeroes
@@ -233,8 +234,9 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
 // ---------------------------------------------------------------------------------------
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr int kFusedMaxRows = 64;               // rows per CTA (one mbarrier each)
+constexpr int kFusedMaxRows = 64;               // rows per CTA
 constexpr int kFusedSmemData = 200 * 1024;      // bytes of x per CTA
+constexpr int kFusedBatch = 6;                  // 16-byte loads in flight per thread
 
 __global__ void __launch_bounds__(kFusedThreads, 1)
     quantize_fused_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M, uint32_t Mpad,
@@ -242,7 +244,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                           uint8_t* __restrict__ scales, unsigned* ws, float* __restrict__ ts_out,
                           uint64_t timeout_ns) {
   extern __shared__ __align__(128) uint8_t xs[];  // rows_per_cta rows of x, K * 2 bytes each
-  __shared__ __align__(8) uint64_t row_bar[kFusedMaxRows];
   __shared__ float inv_tab[128];
   __shared__ uint32_t code_tab[128];
   __shared__ uint32_t warp_max[kFusedWarps];
@@ -256,31 +257,31 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
 
   if (threadIdx.x == 0) failed = 0;
-  if (threadIdx.x < n_real) mbar_init(smem_u32(&row_bar[threadIdx.x]), 1);
-  fence_mbarrier_init();
-  __syncthreads();
-  // warp w copies and then reduces rows w, w + 32, ...
-  if (lane == 0) {
-    const uint64_t pol = policy_evict_first();
-    for (uint32_t i = warp; i < n_real; i += kFusedWarps) {
-      const uint32_t bar = smem_u32(&row_bar[i]);
-      mbar_arrive_expect_tx(bar, row_bytes);
-      bulk_load_hint(smem_u32(xs + i * row_bytes), x + (uint64_t)(r0 + i) * ldx, row_bytes, bar, pol);
-    }
-  }
-
+  // 16-byte chunk c of the CTA's rows: row c / vpr, column chunk c % vpr; in shared memory
+  // the rows are contiguous, so chunk c sits at byte 16 c
+  const uint32_t vpr = K / 8u;
+  const uint32_t nchunks = n_real * vpr;
   uint32_t m = 0u;
-  bool ok = true;
-  for (uint32_t i = warp; i < n_real && ok; i += kFusedWarps) {
-    ok = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&row_bar[i]), 0u, timeout_ns, nullptr));
-    if (!ok) break;
-    const uint4* row = reinterpret_cast<const uint4*>(xs + i * row_bytes);
-    for (uint32_t v = lane; v < K / 8u; v += 32u) {
-      const uint4 q = row[v];
-      m = bf16x2_max_abs(m, bf16x2_max_abs(bf16x2_max_abs(q.x, q.y), bf16x2_max_abs(q.z, q.w)));
+  for (uint32_t c0 = threadIdx.x; c0 < nchunks; c0 += kFusedBatch * kFusedThreads) {
+    uint4 v[kFusedBatch];
+#pragma unroll
+    for (int j = 0; j < kFusedBatch; ++j) {
+      const uint32_t c = c0 + j * kFusedThreads;
+      v[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < nchunks) {
+        const uint32_t r = c / vpr;
+        v[j] = ld_nc_v4(x + (uint64_t)(r0 + r) * ldx + (c - r * vpr) * 8u);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kFusedBatch; ++j) {
+      const uint32_t c = c0 + j * kFusedThreads;
+      if (c < nchunks) {
+        m = bf16x2_max_abs(m, bf16x2_max_abs(bf16x2_max_abs(v[j].x, v[j].y), bf16x2_max_abs(v[j].z, v[j].w)));
+        reinterpret_cast<uint4*>(xs)[c] = v[j];
+      }
     }
   }
-  if (!ok && lane == 0) failed = 1;
   uint32_t h = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
   h = __reduce_max_sync(0xFFFFFFFFu, h);
   if (lane == 0) warp_max[warp] = h;
@@ -350,9 +351,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    // copies still in flight (after a failed wait) must land before the CTA exits
-    if (failed)
-      for (uint32_t i = 0; i < n_real; ++i) (void)mbar_wait(smem_u32(&row_bar[i]), 0u, timeout_ns, nullptr);
     // every CTA that departs has passed the grid barrier and read the words; the last one
     // to depart resets them for the next call
     if (atomicAdd(ws + 2, 1u) == gridDim.x - 1u) {

@@ -94,12 +94,13 @@ class DitBlockLinears:
     # ------------------------------------------------------------------------------------
     def calibrate(self, x: torch.Tensor, ts_mid: Optional[torch.Tensor] = None) -> torch.Tensor:
         """Sets the static NVFP4 scale of the up-projection output: ``ts_mid`` (a one-element
-        fp32 device tensor) if given, else amax / 2688 of that output on input ``x`` (one
-        pass of the first layers with a bf16 up-projection output)."""
+        fp32 device tensor) if given, else the tensor scale amax / 2688 that nvfp4_quantize
+        computes for that output on input ``x`` (one pass of the first layers with a bf16
+        up-projection output, then the library's quantizer, whose tensor scale is kept)."""
         if ts_mid is None:
             o = self.out_proj(self.attention(self.qkv_rmsnorm(x)))
             u = nvfp4_gemm(nvfp4_quantize(o), self.qb["up"], "gated_silu", bias=self.bias["up"])
-            ts_mid = (u.float().abs().max() / 2688.0).reshape(1)
+            ts_mid = nvfp4_quantize(u).ts
         self.ts_mid = ts_mid.to(self.device, torch.float32).reshape(1).contiguous()
         return self.ts_mid
 

@@ -16,7 +16,7 @@ import nvfp4_gemm_act_b300 as nv
 from nvfp4_gemm_act_b300 import workloads as W
 from oracle import nvfp4_ref as R
 
-from parity import to_np_f32
+from parity import assert_attention_close, attention_oracle, to_np_f32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -24,12 +24,7 @@ HD = 256
 
 
 def _ref(qkv: np.ndarray, heads: int, rows=None) -> np.ndarray:
-    M = qkv.shape[0]
-    H = heads * HD
-    t = qkv.reshape(M, 3, heads, HD).transpose(1, 2, 0, 3)  # [3, heads, M, HD]
-    q = t[0] if rows is None else t[0][:, rows]
-    o = R.attention_ref(q, t[1], t[2])                      # [heads, rows, HD]
-    return o.transpose(1, 0, 2).reshape(-1, H)
+    return attention_oracle(qkv, heads, HD, rows)
 
 
 def _run(qkv: torch.Tensor, heads: int) -> np.ndarray:
@@ -41,13 +36,7 @@ def _run(qkv: torch.Tensor, heads: int) -> np.ndarray:
 
 
 def _check(got, ref, what):
-    rms = float(np.sqrt(np.mean(ref ** 2)))
-    assert np.all(np.isfinite(got)), what
-    rel = float(np.sqrt(np.mean((got - ref) ** 2))) / rms
-    worst = float(np.max(np.abs(got - ref) - R.bf16_ulp(ref)))
-    assert rel <= 5e-3, f"{what}: rms error {rel:.2e} of rms"
-    assert worst <= 5e-2 * rms, f"{what}: max error {worst / rms:.2e} of rms"
-    return rel
+    return assert_attention_close(got, ref, what)
 
 
 @pytest.mark.parametrize("M,heads,q_scale", [(200, 2, 1.0), (1, 1, 1.0), (64, 1, 1.0), (65, 1, 1.0),

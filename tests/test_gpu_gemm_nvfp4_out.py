@@ -5,9 +5,9 @@ for the next layer (through the C ABI).
 Expected values come from the oracle alone: its fp64 epilogue output, rounded to bf16, then
 its block quantizer with the same static scale. The GPU's fp32 epilogue value can round to
 the neighbouring bf16 value where the oracle's value lies within fp32 error of a bf16 rounding
-midpoint; a 16-block whose oracle values all lie farther than 1e-5 (relative) from every such
-midpoint has the same bf16 inputs on both sides and so must match bit for bit. The other
-blocks (a few percent) are compared after dequantization.
+midpoint. The same GEMM's fp32 output (held to the fp32 bar) shows which: a 16-block whose 16
+values round to the same bf16 on both sides has identical quantizer inputs and must match bit
+for bit; the other blocks (a few percent) are compared after dequantization.
 """
 import numpy as np
 import pytest
@@ -17,40 +17,10 @@ import nvfp4_gemm_act_b300 as nv
 from nvfp4_gemm_act_b300 import workloads as W
 from oracle import nvfp4_ref as R
 
-from parity import Case, assert_fp32_close, gpu_nvfp4_to_np, to_np_f32
+from parity import Case, assert_nvfp4_out_close as _check_against_oracle, gpu_nvfp4_to_np, to_np_f32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-SAFE_REL = 1e-5
-
-
-def _safe_blocks(y_ref: np.ndarray) -> np.ndarray:
-    """[rows, W/16] bool: every value of the block lies > SAFE_REL * |y| from a bf16 midpoint."""
-    rn = R.round_to_bf16(y_ref)
-    dist = R.bf16_ulp(rn) / 2 - np.abs(y_ref - rn)
-    safe = dist > SAFE_REL * np.abs(y_ref) + 1e-300
-    return safe.reshape(y_ref.shape[0], -1, 16).all(axis=2)
-
-
-def _check_against_oracle(got, y_ref, ts_out, what):
-    gc, gs, gt = got
-    rc, rs, _ = R.quantize_ref(R.round_to_bf16(y_ref), np.float32(ts_out))
-    assert np.float32(gt) == np.float32(ts_out)
-    safe = _safe_blocks(y_ref)
-    assert safe.mean() > 0.9, f"{what}: only {safe.mean():.3f} of the blocks are exactly checkable"
-    bad_s = np.argwhere((gs != rs) & safe)
-    assert bad_s.size == 0, f"{what}: scale mismatch in exactly checkable blocks {bad_s[:5].tolist()}"
-    code_safe = np.repeat(safe, 16, axis=1)
-    bad_c = np.argwhere((gc != rc) & code_safe)
-    assert bad_c.size == 0, f"{what}: code mismatch in exactly checkable blocks {bad_c[:5].tolist()}"
-    # the rest: dequantized values within two steps of the coarser of the two grids
-    dq_g = R.dequantize_ref(gc, gs, ts_out)
-    dq_r = R.dequantize_ref(rc, rs, ts_out)
-    step = 2.0 * np.maximum(np.repeat(R.e4m3_decode(gs), 16, axis=1), np.repeat(R.e4m3_decode(rs), 16, axis=1))
-    assert np.all(np.abs(dq_g - dq_r) <= 2 * step * float(ts_out) + 1e-30), f"{what}: far-off block"
-    return safe.mean()
-
-
 def _run(w: W.Workload, ts_scale: float = 1.0, rows=None):
     c = Case(w)
     ref = c.oracle_y(rows)
@@ -76,9 +46,12 @@ def _run(w: W.Workload, ts_scale: float = 1.0, rows=None):
     assert np.array_equal(got[1], two[1]) and np.array_equal(got[0], two[0]), \
         "fused NVFP4 output differs from bf16 output + nvfp4_quantize"
     assert np.array_equal(q.scales.cpu().numpy(), q2.scales.cpu().numpy()), "scale padding differs"
+    # the fp32 values the NVFP4 output rounds to bf16 (the same kernel, fp32 output mode)
+    y32 = to_np_f32(nv.nvfp4_gemm(qa, qb, w.epilogue, out_dtype=torch.float32, **kw)).astype(np.float64)
     if rows is not None:
         got = (got[0][rows], got[1][rows], got[2])
-    return got, ref, ts_out
+        y32 = y32[rows]
+    return got, ref, ts_out, y32
 
 
 @pytest.mark.parametrize("epi,M,N,K", [("bias", 256, 512, 512), ("gated_silu", 300, 512, 320),
@@ -86,22 +59,22 @@ def _run(w: W.Workload, ts_scale: float = 1.0, rows=None):
 def test_nvfp4_out_small(epi, M, N, K):
     norm_cols = 512 if epi == "head_rmsnorm" else 0
     w = W.Workload(f"q_{epi}", M, K, N, epi, seed=M + N, norm_cols=norm_cols, head_dim=128)
-    got, ref, ts = _run(w)
-    _check_against_oracle(got, ref, ts, f"{epi} M={M}")
+    got, ref, ts, y32 = _run(w)
+    _check_against_oracle(got, ref, ts, f"{epi} M={M}", y_gpu32=y32)
 
 
 @pytest.mark.parametrize("ts_scale", [0.05, 20.0])
 def test_nvfp4_out_saturating_and_coarse_static_scales(ts_scale):
     # a static scale far too small (block scales saturate at 448, codes at 6) or too large
     w = W.Workload("q_sat", 128, 256, 256, "bias", seed=31)
-    got, ref, ts = _run(w, ts_scale=ts_scale)
-    _check_against_oracle(got, ref, ts, f"ts x{ts_scale}")
+    got, ref, ts, y32 = _run(w, ts_scale=ts_scale)
+    _check_against_oracle(got, ref, ts, f"ts x{ts_scale}", y_gpu32=y32)
 
 
 def test_nvfp4_out_up_projection_full_size_sampled_rows():
     rows = np.unique(np.concatenate([[0, 127, 128, 4095, 4607], np.random.default_rng(17).integers(0, 4608, 19)]))
-    got, ref, ts = _run(W.GATED_UP, rows=rows)
-    _check_against_oracle(got, ref, ts, "gated up-projection 4608x12288 sampled")
+    got, ref, ts, y32 = _run(W.GATED_UP, rows=rows)
+    _check_against_oracle(got, ref, ts, "gated up-projection 4608x12288 sampled", y_gpu32=y32)
 
 
 def test_up_down_chain_through_nvfp4():
