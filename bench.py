@@ -5,7 +5,9 @@ M = 4608 tokens, with the weights already packed (offline) and resident in HBM:
     quantize X [4608, 3072]  -> QKV GEMM [x3072 -> 9216]   + per-head RMSNorm epilogue
     quantize X [4608, 3072]  -> up  GEMM [x3072 -> 24576]  + gated-SiLU epilogue (-> 12288)
     quantize X [4608, 12288] -> down GEMM [x12288 -> 3072] + bias epilogue
-Every op is a kernel of libnvfp4.so called through the C ABI (9 kernels per step).
+Every op is a kernel of libnvfp4.so called through the C ABI: 7 launches per step (the two
+smaller activations quantized by one single-pass launch each, the down-projection input by
+an amax pass and an encode pass, and the three GEMMs).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -246,17 +248,32 @@ def kernel_source_hash(op: str) -> str:
 
 
 def read_traffic(op: str):
-    """DRAM bytes per launch of `op` from the committed ncu summary, if it was taken on the
-    current kernel sources (the file records the source hash); else None."""
+    """(DRAM bytes per launch of `op`, their provenance) from the committed ncu summary if it
+    was taken on the current kernel sources (the file records the source hash); else
+    (None, why)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    if not os.path.exists(path):
-        return None
     src = kernel_source_hash(op)
-    for line in open(path):
-        parts = line.split()
-        if len(parts) >= 3 and not line.startswith("#") and parts[0] == op and parts[1] == src:
-            return float(parts[2])
-    return None
+    if os.path.exists(path):
+        for line in open(path):
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == op and parts[1] == src:
+                return float(parts[2]), (f"ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, one launch) "
+                                         f"recorded in profiles/dram_traffic.txt for kernel-source hash {src}")
+    return None, f"no ncu capture recorded for kernel-source hash {src}"
+
+
+def instruction_ceiling(nv, torch, dev, iters=20000):
+    """The NVFP4 MMA instruction ceiling measured now (nvfp4_debug_mma_rate): back-to-back
+    tcgen05.mma kind::mxf4nvf4.block16 M256 N256 K64 on every SM pair; TFLOP/s = FLOPs of all
+    pairs / the slowest pair's time."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pairs = sms // 2
+    nv.nvfp4_debug_mma_rate("nvfp4", 2, 256, iters, pairs)  # warm-up
+    r = nv.nvfp4_debug_mma_rate("nvfp4", 2, 256, iters, pairs)
+    torch.cuda.synchronize()
+    r = r.cpu().numpy()
+    flops = 2.0 * 256 * 256 * 64 * iters * pairs
+    return flops / (float(r[:, 1].max()) * 1e-9) / 1e12
 
 
 def measured_peaks():
@@ -409,7 +426,8 @@ def run_ours(args, world, rank, local):
             e["frac_of_hbm_measured"] = round(by / (ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4)
         breakdown[name] = e
     gemm_ms = sum(mean_op[i] for i, o in enumerate(ops) if o[2])
-    traffic = read_traffic(dom_name)
+    traffic, traffic_source = read_traffic(dom_name)
+    ceiling = instruction_ceiling(nv, torch, dev)
     # the down-projection input's quantizer with a static tensor scale (one streaming pass; the
     # step uses the dynamic scale: amax pass + quantize pass), timed alone, L2 flushed first
     down = [l for l in layers if l.w.name == "down_bias"]
@@ -449,7 +467,10 @@ def run_ours(args, world, rank, local):
                      "frac": round(achieved / fp4_peak, 4),
                      "peak_basis": f"{peaks_src} bf16 burst {peaks['bf16_tflops']} x {FP4_OVER_BF16:g} (nominal fp4:bf16)",
                      "frac_of_15pf": round(achieved / (NOMINAL_FP4_PF * 1e3), 4),
-                     "traffic": traffic, "algorithmic_bytes": dom_bytes},
+                     "instruction_ceiling": round(ceiling, 1),
+                     "frac_of_instruction_ceiling": round(achieved / ceiling, 4),
+                     "instruction_ceiling_basis": "measured in this run: back-to-back tcgen05.mma kind::mxf4nvf4.block16 M256 N256 K64 on all SM pairs (nvfp4_debug_mma_rate), the fastest any NVFP4 GEMM here can go",
+                     "traffic": traffic, "traffic_source": traffic_source, "algorithmic_bytes": dom_bytes},
         "gemm_only_tflops": round(flops_step / (gemm_ms / 1e3) / 1e12, 1),
         "step_ms_min_median": [round(float(step_ms.min()), 5), round(float(np.median(step_ms)), 5)],
         "eager_ms_per_step": round(float(eager_step_ms.mean()), 5),

@@ -312,6 +312,23 @@ NVFP4_API const char *nvfp4_status_string(nvfp4_status status);
 NVFP4_API nvfp4_status nvfp4_debug_wait_timeout(int *device_error, int64_t timeout_ns,
                                       nvfp4_stream_t stream);
 
+/*
+ * Debug build -- the same library compiled with -DNVFP4_DEBUG (libnvfp4_debug.so, built beside
+ * libnvfp4.so). Its kernels check the indices of their stores (and of the few loads whose
+ * index is computed): output rows and columns against M and the output width, the
+ * 16-byte alignment of every TMA store's first coordinate, code and scale offsets against
+ * the buffers' sizes, shared-memory offsets against the rows a CTA holds, bias indices against
+ * N. A failed check skips that access and is counted on the device; nothing traps, so the
+ * context stays usable. Release builds compile the checks out.
+ */
+
+/* 1 if this library was built with the index checks, 0 otherwise. Needs no GPU. */
+NVFP4_API int nvfp4_debug_build(void);
+
+/* Synchronizes the device, writes to *count the number of index checks that failed in the
+ * library's kernels since the last call (always 0 in a release build), and clears it. */
+NVFP4_API nvfp4_status nvfp4_debug_index_failures(int64_t *count);
+
 /* Instruction kinds of nvfp4_debug_mma_rate. */
 typedef enum nvfp4_probe_kind {
   NVFP4_PROBE_NVFP4 = 0,  /* tcgen05.mma kind::mxf4nvf4.block_scale.block16, K = 64 */

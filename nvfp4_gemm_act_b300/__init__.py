@@ -19,6 +19,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
+# the same library built with the kernels' index checks (nvfp4_debug_build() == 1)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libnvfp4_debug.so")
 
 EPILOGUES = {"bias": 0, "head_rmsnorm": 1, "gated_silu": 2}
 OUT_DTYPES = {torch.bfloat16: 0, torch.float32: 1}
@@ -43,6 +45,8 @@ _SIGS = {
     "nvfp4_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "nvfp4_debug_wait_timeout": (ctypes.c_int, [_P, _I64, _P]),
     "nvfp4_quantize_noalloc": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "nvfp4_debug_build": (ctypes.c_int, []),
+    "nvfp4_debug_index_failures": (ctypes.c_int, [_P]),
     "nvfp4_debug_mma_rate": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _I64, ctypes.c_int, _P,
                                             _P, _P]),
     "fp8_quantize": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
@@ -60,19 +64,23 @@ class Nvfp4Error(RuntimeError):
         self.status = status
 
 
+def load_library(path: str) -> ctypes.CDLL:
+    """Loads a build of the C-ABI library and declares every entry point's signature."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing; build it with `python -m nvfp4_gemm_act_b300.build`")
+    L = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """The loaded C-ABI library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing; build it with "
-                               "`python -m nvfp4_gemm_act_b300.build`")
-        L = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGS.items():
-            f = getattr(L, name)
-            f.restype = res
-            f.argtypes = args
-        _lib = L
+        _lib = load_library(LIB_PATH)
     return _lib
 
 

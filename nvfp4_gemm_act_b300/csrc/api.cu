@@ -400,6 +400,25 @@ nvfp4_status nvfp4_debug_wait_timeout(int* device_error, int64_t timeout_ns, nvf
                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int nvfp4_debug_build(void) {
+#ifdef NVFP4_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+nvfp4_status nvfp4_debug_index_failures(int64_t* count) {
+  if (count == nullptr) return NVFP4_ERR_NULL;
+  if (nvfp4_status st = check_device(); st != NVFP4_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  unsigned q = 0u, g = 0u;
+  if (nvfp4::take_index_failures_quantize(&q) != cudaSuccess || nvfp4::take_index_failures_gemm(&g) != cudaSuccess)
+    return NVFP4_ERR_LAUNCH;
+  *count = static_cast<int64_t>(q) + static_cast<int64_t>(g);
+  return NVFP4_OK;
+}
+
 nvfp4_status nvfp4_debug_mma_rate(nvfp4_probe_kind kind, int cta_group, int n, int64_t iters, int ctas,
                                   int64_t* out, int* device_error, nvfp4_stream_t stream) {
   if (kind != NVFP4_PROBE_NVFP4 && kind != NVFP4_PROBE_FP8 && kind != NVFP4_PROBE_BF16) return NVFP4_ERR_ARG;

@@ -113,7 +113,7 @@ static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 constexpr uint32_t kBarEpiParams = 1;    // named barriers among the epilogue warps
-constexpr uint32_t kBarEpiXch = 2;
+constexpr uint32_t kBarEpiXch0 = 2;      // + lane quarter: the two warps sharing a quarter (ids 2-5)
 
 // Instruction descriptor for kind::mxf4nvf4: A and B E2M1 (format 1), K-major, dense,
 // UE4M3 scales (bit 23 = 0), scale-factor ids 0, N >> 3 at bits 17-22, M >> 4 at 24-28.
@@ -203,7 +203,9 @@ __device__ __forceinline__ void store_rows(const EpiParams& p, const void* tm_ou
     __syncwarp();
     if (lane == 0) {
       // rows past M and columns past the width are clipped by the tensor map
-      tma_store_2d(tm_out, buf, col0 + c, row0);
+      if (NVFP4_INDEX_OK(row0 >= 0 && row0 < p.M && (row0 & 31) == 0 && col0 + c >= 0 && col0 + c < width &&
+                         ((col0 + c) * (bf16 ? 2 : 4)) % 16 == 0))
+        tma_store_2d(tm_out, buf, col0 + c, row0);
       bulk_commit_group();
     }
   }
@@ -231,10 +233,12 @@ __device__ __forceinline__ void store_rows_nvfp4(const EpiParams& p, const Quant
     if (real) {
       uint2 c;
       stored = quantize_block(lo, hi, qo.sr, qo.inv_tab, qo.code_tab, c);
-      *reinterpret_cast<uint2*>(p.out_codes + (int64_t)row * (width >> 1) + (col >> 1)) = c;
+      if (NVFP4_INDEX_OK(row >= 0 && col >= 0 && (col & 15) == 0 && col + 16 <= width))
+        *reinterpret_cast<uint2*>(p.out_codes + (int64_t)row * (width >> 1) + (col >> 1)) = c;
     }
-    p.out_scales[scale_offset(static_cast<uint32_t>(row), static_cast<uint32_t>(col >> 4), gpr)] =
-        static_cast<uint8_t>(stored);
+    const uint32_t soff = scale_offset(static_cast<uint32_t>(row), static_cast<uint32_t>(col >> 4), gpr);
+    if (NVFP4_INDEX_OK(row >= 0 && static_cast<int64_t>(soff) < static_cast<int64_t>((p.M + 127) / 128) * gpr * 512))
+      p.out_scales[soff] = static_cast<uint8_t>(stored);
   }
 }
 
@@ -284,8 +288,11 @@ __device__ __forceinline__ void epilogue_row(const EpiParams& p, const QuantOut&
     } else {
       float s = (cs[0] + cs[1]) + (cs[2] + cs[3]);
       if (hd == 256) {  // the head spans both halves of the tile row
+        // only the two warps of this lane quarter (one per half) exchange their row sums; the
+        // slots are free again by the next tile: every epilogue warp passes the per-tile
+        // parameter barrier after reading its partner's sum
         xch[half * kBM + row_local] = s;
-        named_bar_sync(kBarEpiXch, kEpiThreads);
+        named_bar_sync(kBarEpiXch0 + static_cast<uint32_t>(row_local >> 5), 64);
         const float o = xch[(half ^ 1) * kBM + row_local];
         s = half == 0 ? s + o : o + s;  // same summation order in both halves
       }
@@ -553,7 +560,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_a, const CUtenso
         if (ep.bias != nullptr && col < ep.N) {
           // gated: packed column 2j is gate column j, 2j+1 is up column N/2 + j
           const int orig = gated ? ((col & 1) ? nhalf + (col >> 1) : (col >> 1)) : col;
-          b = __ldg(ep.bias + orig);
+          if (NVFP4_INDEX_OK(orig >= 0 && orig < ep.N)) b = __ldg(ep.bias + orig);
         }
         if (ep.epi == NVFP4_EPI_HEAD_RMSNORM && col < ep.norm_cols) g = __ldg(ep.gamma + col);
         bias_s[et] = b;
@@ -773,6 +780,23 @@ nvfp4_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
             : cudaLaunchKernelEx(&cfg, gemm_nvfp4_kernel, tm_a, tm_b, tm_sfa, tm_sfb, tm_out, K, num_m,
                                  num_pair_tiles, ep, a.err, limit);
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH;
+}
+
+
+// Failed index checks counted by this file's kernels since the last call (debug builds; always
+// 0 otherwise); reading clears the counter. Call with the device idle.
+cudaError_t take_index_failures_gemm(unsigned* n) {
+#ifdef NVFP4_DEBUG
+  unsigned v = 0u;
+  const unsigned zero = 0u;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_index_failures, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_index_failures, &zero, sizeof(zero));
+  *n = v;
+  return e;
+#else
+  *n = 0u;
+  return cudaSuccess;
+#endif
 }
 
 }  // namespace nvfp4

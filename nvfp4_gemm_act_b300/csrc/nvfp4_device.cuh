@@ -35,6 +35,22 @@ __device__ __forceinline__ void report_error(int* err, int code) {
   if (err != nullptr) atomicCAS(err, 0, code);
 }
 
+// Debug builds (-DNVFP4_DEBUG): NVFP4_INDEX_OK(cond) guards a store (or load) of the
+// epilogues and the quantizers; a false condition skips the access and is counted in this
+// translation unit's device counter (each .cu file is its own device module), which
+// nvfp4_debug_index_failures reads. Nothing traps. Release builds compile the checks out: the
+// macro is `true` and its condition is not evaluated.
+#ifdef NVFP4_DEBUG
+static __device__ unsigned int g_index_failures;
+__device__ __forceinline__ bool index_check(bool ok) {
+  if (!ok) atomicAdd(&g_index_failures, 1u);
+  return ok;
+}
+#define NVFP4_INDEX_OK(cond) (::nvfp4::index_check(cond))
+#else
+#define NVFP4_INDEX_OK(cond) true
+#endif
+
 // ---------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------

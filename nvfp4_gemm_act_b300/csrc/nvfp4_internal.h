@@ -89,6 +89,10 @@ nvfp4_status launch_attention(const void* qkv, int64_t M, int64_t ld_qkv, int he
 
 cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t s);
 
+// Failed index checks of the quantize / GEMM kernels since the last call (debug builds), cleared.
+cudaError_t take_index_failures_quantize(unsigned* n);
+cudaError_t take_index_failures_gemm(unsigned* n);
+
 // Validated arguments of nvfp4_debug_mma_rate in, the probe kernel launched.
 nvfp4_status launch_mma_probe(int kind, int cta_group, int n, int iters, int ctas, long long* out, int* err,
                               cudaStream_t s);

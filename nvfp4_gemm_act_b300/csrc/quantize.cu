@@ -192,10 +192,14 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
         if (ru < M) {
           uint2 c;
           stored = quantize_block(lo[u], hi[u], sr, inv_tab, code_tab, c);
-          *reinterpret_cast<uint2*>(codes + ru * row_code_bytes + blk * 8u) = c;
+          if (NVFP4_INDEX_OK(blk < blocks_per_row &&
+                             (uint64_t)ru * row_code_bytes + blk * 8u + 8u <= (uint64_t)M * row_code_bytes))
+            *reinterpret_cast<uint2*>(codes + ru * row_code_bytes + blk * 8u) = c;
         }
-        scales[((ru >> 7) * gpr + static_cast<uint32_t>(chunk[u]) * 8u) * 512u + (ru & 31u) * 16u +
-               ((ru >> 5) & 3u) * 4u + lane_sf] = static_cast<uint8_t>(stored);
+        const uint64_t sidx = ((ru >> 7) * gpr + static_cast<uint32_t>(chunk[u]) * 8u) * 512u + (ru & 31u) * 16u +
+                              ((ru >> 5) & 3u) * 4u + lane_sf;
+        if (NVFP4_INDEX_OK(sidx < (uint64_t)((M + 127u) / 128u) * gpr * 512u && sidx == scale_offset(ru, blk, gpr)))
+          scales[sidx] = static_cast<uint8_t>(stored);
       }
       chunk[u] -= step_chunks;
       row[u] -= step_rows;
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         valid[u] = it < items && bb[u] < bpr;
         data[u] = valid[u] && i < n_real;
         lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (data[u]) {
+        if (data[u] && NVFP4_INDEX_OK(i * row_bytes + bb[u] * 32u + 32u <= rows_per_cta * row_bytes)) {
           const uint4* src = reinterpret_cast<const uint4*>(xs + i * row_bytes + bb[u] * 32u);
           lo[u] = src[0];
           hi[u] = src[1];
@@ -343,9 +347,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         if (data[u]) {
           uint2 c;
           stored = quantize_block(lo[u], hi[u], sr, inv_tab, code_tab, c);
-          *reinterpret_cast<uint2*>(codes + rr[u] * row_code_bytes + bb[u] * 8u) = c;
+          if (NVFP4_INDEX_OK(rr[u] < M && bb[u] < bpr))
+            *reinterpret_cast<uint2*>(codes + rr[u] * row_code_bytes + bb[u] * 8u) = c;
         }
-        scales[scale_offset(rr[u], bb[u], gpr)] = static_cast<uint8_t>(stored);
+        if (NVFP4_INDEX_OK(rr[u] < Mpad && bb[u] < bpr))
+          scales[scale_offset(rr[u], bb[u], gpr)] = static_cast<uint8_t>(stored);
       }
     }
   }
@@ -417,6 +423,7 @@ __global__ void __launch_bounds__(256)
   const uint32_t half = N >> 1;
   const uint32_t p = kGated ? (n < half ? 2u * n : 2u * (n - half) + 1u) : n;
   const uint32_t kb = (k0 >> 4) + b;
+  if (!NVFP4_INDEX_OK(p < N && kb < (K >> 4))) return;
   *reinterpret_cast<uint2*>(codes + (uint64_t)p * (K >> 1) + (kb << 3)) = make_uint2(lo, hi);
   const uint32_t gpr = K >> 6;
   scales[((p >> 7) * gpr + (kb >> 2)) * 512u + (p & 31u) * 16u + ((p >> 5) & 3u) * 4u + (kb & 3u)] =
@@ -471,7 +478,7 @@ __global__ void __launch_bounds__(kFp8Threads)
       }
       out = encode_e4m3x16(v, inv);
     }
-    *reinterpret_cast<uint4*>(codes + r * K + c) = out;
+    if (NVFP4_INDEX_OK(r < M && c + 16u <= K)) *reinterpret_cast<uint4*>(codes + r * K + c) = out;
   }
   if (ts_in == nullptr) {
     __syncthreads();  // every thread of this CTA has read the amax word
@@ -525,7 +532,7 @@ __global__ void __launch_bounds__(256)
   const uint4 out = live ? encode_e4m3x16(vals, inv) : make_uint4(0u, 0u, 0u, 0u);
   const uint32_t half = N >> 1;
   const uint32_t p = kGated ? (n < half ? 2u * n : 2u * (n - half) + 1u) : n;
-  *reinterpret_cast<uint4*>(codes + (uint64_t)p * K + k0 + b * 16u) = out;
+  if (NVFP4_INDEX_OK(p < N && k0 + b * 16u + 16u <= K)) *reinterpret_cast<uint4*>(codes + (uint64_t)p * K + k0 + b * 16u) = out;
 }
 
 __global__ void wait_timeout_kernel(int* err, uint64_t limit_ns) {
@@ -668,6 +675,23 @@ cudaError_t launch_fp8_pack_weights(const void* w, int64_t K, int64_t N, bool ga
 cudaError_t launch_wait_timeout(int* err, uint64_t limit_ns, cudaStream_t s) {
   wait_timeout_kernel<<<1, 32, 0, s>>>(err, limit_ns);
   return cudaGetLastError();
+}
+
+
+// Failed index checks counted by this file's kernels since the last call (debug builds; always
+// 0 otherwise); reading clears the counter. Call with the device idle.
+cudaError_t take_index_failures_quantize(unsigned* n) {
+#ifdef NVFP4_DEBUG
+  unsigned v = 0u;
+  const unsigned zero = 0u;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_index_failures, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_index_failures, &zero, sizeof(zero));
+  *n = v;
+  return e;
+#else
+  *n = 0u;
+  return cudaSuccess;
+#endif
 }
 
 }  // namespace nvfp4

@@ -240,3 +240,15 @@ def test_binding_refuses_host_tensors():
         nv.fp8_quantize(x)
     with pytest.raises(ValueError):
         nv.attention(torch.zeros((64, 3 * 256), dtype=torch.bfloat16), 1)
+
+
+def test_debug_build_flag_and_exports():
+    # the release library compiles the index checks out; the debug build has them and exports
+    # the same entry points
+    assert nv.lib().nvfp4_debug_build() == 0
+    if os.path.exists(nv.DEBUG_LIB_PATH):
+        assert nv.load_library(nv.DEBUG_LIB_PATH).nvfp4_debug_build() == 1
+        out = os.popen(f"nm -D --defined-only {nv.DEBUG_LIB_PATH}").read()
+        exported = {l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("nvfp4")}
+        assert exported == set(header_functions())
+    assert nv.lib().nvfp4_debug_index_failures(None) == ERR_NULL
