@@ -41,15 +41,18 @@ __host__ __device__ constexpr uint32_t idesc_for(int kind, int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | shape;
 }
 
-__device__ __forceinline__ void mma_issue(int kind, bool pair, uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t sfa, uint32_t sfb, uint32_t acc) {
-  if (kind == NVFP4_PROBE_NVFP4) {
-    if (pair)
+// The kind and the CTA-group form are template parameters, so the issue loop holds nothing but
+// the descriptor arithmetic and the MMAs themselves (as a GEMM's mainloop does).
+template <int kKind, bool pair>
+__device__ __forceinline__ void mma_issue(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                          uint32_t sfb, uint32_t acc) {
+  if constexpr (kKind == NVFP4_PROBE_NVFP4) {
+    if constexpr (pair)
       mma_nvf4_pair(d, a, b, idesc, sfa, sfb, acc);
     else
       mma_nvf4(d, a, b, idesc, sfa, sfb, acc);
-  } else if (kind == NVFP4_PROBE_FP8) {
-    if (pair) {
+  } else if constexpr (kKind == NVFP4_PROBE_FP8) {
+    if constexpr (pair) {
       mma_f8_pair(d, a, b, idesc, acc);
     } else {
       asm volatile(
@@ -59,7 +62,7 @@ __device__ __forceinline__ void mma_issue(int kind, bool pair, uint32_t d, uint6
           : "memory");
     }
   } else {
-    if (pair) {
+    if constexpr (pair) {
       asm volatile(
           "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
           "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
@@ -83,9 +86,9 @@ __device__ __forceinline__ uint64_t clock64_now() {
 
 // out[2 c] = SM cycles, out[2 c + 1] = ns of the batch of CTA (pair) c; written by the issuing
 // CTA only.
-template <bool kPair>
+template <bool kPair, int kind>
 __global__ void __launch_bounds__(kProbeThreads, 1)
-    mma_probe_kernel(int kind, int n, int iters, long long* out, int* err, uint64_t timeout_ns) {
+    mma_probe_kernel(int n, int iters, long long* out, int* err, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -154,8 +157,8 @@ __global__ void __launch_bounds__(kProbeThreads, 1)
         const int j = i & 3;
         const uint64_t a = smem_desc(sbase + kOffA + j * 32, 16, 1024, kSwizzle128B);
         const uint64_t b = smem_desc(sbase + kOffB + j * 32, 16, 1024, kSwizzle128B);
-        mma_issue(kind, kPair, tmem, a, b, idesc, tmem + kSfCol + j * 4, tmem + kSfCol + 16 + j * 8,
-                  i > 0 ? 1u : 0u);
+        mma_issue<kind, kPair>(tmem, a, b, idesc, tmem + kSfCol + j * 4, tmem + kSfCol + 16 + j * 8,
+                               i > 0 ? 1u : 0u);
       }
       if (kPair)
         tc_commit_pair_mc(bar_done, 0x3);
@@ -184,19 +187,15 @@ __global__ void __launch_bounds__(kProbeThreads, 1)
   }
 }
 
-}  // namespace
-
-nvfp4_status launch_mma_probe(int kind, int cta_group, int n, int iters, int ctas, long long* out, int* err,
-                              cudaStream_t s) {
-  static const cudaError_t ready1 =
-      cudaFuncSetAttribute(mma_probe_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem);
-  static const cudaError_t ready2 =
-      cudaFuncSetAttribute(mma_probe_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem);
-  if ((cta_group == 2 ? ready2 : ready1) != cudaSuccess) return NVFP4_ERR_LAUNCH;
+template <bool kPair, int kKind>
+nvfp4_status launch_probe_form(int n, int iters, int ctas, long long* out, int* err, cudaStream_t s) {
+  static const cudaError_t ready =
+      cudaFuncSetAttribute(mma_probe_kernel<kPair, kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem);
+  if (ready != cudaSuccess) return NVFP4_ERR_LAUNCH;
   const uint64_t limit = wait_timeout_ns();
   cudaError_t e;
-  if (cta_group == 1) {
-    mma_probe_kernel<false><<<ctas, kProbeThreads, kProbeSmem, s>>>(kind, n, iters, out, err, limit);
+  if constexpr (!kPair) {
+    mma_probe_kernel<false, kKind><<<ctas, kProbeThreads, kProbeSmem, s>>>(n, iters, out, err, limit);
     e = cudaGetLastError();
   } else {
     cudaLaunchConfig_t cfg = {};
@@ -211,9 +210,27 @@ nvfp4_status launch_mma_probe(int kind, int cta_group, int n, int iters, int cta
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, mma_probe_kernel<true>, kind, n, iters, out, err, limit);
+    e = cudaLaunchKernelEx(&cfg, mma_probe_kernel<true, kKind>, n, iters, out, err, limit);
   }
   return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH;
+}
+
+}  // namespace
+
+nvfp4_status launch_mma_probe(int kind, int cta_group, int n, int iters, int ctas, long long* out, int* err,
+                              cudaStream_t s) {
+  const bool pair = cta_group == 2;
+  switch (kind) {
+    case NVFP4_PROBE_NVFP4:
+      return pair ? launch_probe_form<true, NVFP4_PROBE_NVFP4>(n, iters, ctas, out, err, s)
+                  : launch_probe_form<false, NVFP4_PROBE_NVFP4>(n, iters, ctas, out, err, s);
+    case NVFP4_PROBE_FP8:
+      return pair ? launch_probe_form<true, NVFP4_PROBE_FP8>(n, iters, ctas, out, err, s)
+                  : launch_probe_form<false, NVFP4_PROBE_FP8>(n, iters, ctas, out, err, s);
+    default:
+      return pair ? launch_probe_form<true, NVFP4_PROBE_BF16>(n, iters, ctas, out, err, s)
+                  : launch_probe_form<false, NVFP4_PROBE_BF16>(n, iters, ctas, out, err, s);
+  }
 }
 
 }  // namespace nvfp4
