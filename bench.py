@@ -548,10 +548,43 @@ def run_e2e(args, layers, dev, dist):
     for l in layers:
         assert nv.nvfp4_get_device_error(l.err) == 0
     t_max, units = aggregate(el, flops * K, dist)
+    floor = copy_floor(hx, dx[0], hy[0], dy[0], s_in, s_out, K)
+    step_ms = t_max / K * 1e3
     return {"value": round(units / t_max / 1e12, 2), "unit": UNIT,
             "h2d_bytes_per_step": int(sum(h.numel() * h.element_size() for h in hx)),
             "d2h_bytes_per_step": int(sum(h.numel() * h.element_size() for h in hy[0])),
-            "steps": K, "pipelined": "H2D / compute / D2H streams, double-buffered"}
+            "steps": K, "pipelined": "H2D / compute / D2H streams, double-buffered",
+            "ms_per_step": round(step_ms, 4),
+            "copy_floor": dict(floor, frac=round(floor["both_ms"] / step_ms, 4))}
+
+
+def copy_floor(hx, dx, hy, dy, s_in, s_out, reps):
+    """The step's copies alone, as the e2e loop issues them (the three inputs host->device on
+    one stream, the three outputs device->host on another), each direction alone and both at
+    once: the time no pipelining can beat, measured in the same run."""
+    import torch
+
+    def run(h2d, d2h):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            if h2d:
+                with torch.cuda.stream(s_in):
+                    for d, h in zip(dx, hx):
+                        d.copy_(h, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s_out):
+                    for h, d in zip(hy, dy):
+                        h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps * 1e3
+
+    run(True, True)  # warm
+    h2d_ms, d2h_ms, both_ms = run(True, False), run(False, True), run(True, True)
+    nin = sum(h.numel() * h.element_size() for h in hx)
+    nout = sum(h.numel() * h.element_size() for h in hy)
+    return {"h2d_gbs": round(nin / h2d_ms / 1e6, 1), "d2h_gbs": round(nout / d2h_ms / 1e6, 1),
+            "both_ms": round(both_ms, 4), "note": "pinned-host copies of the step alone; frac = both_ms / ms_per_step"}
 
 
 # ---------------------------------------------------------------------------------------
