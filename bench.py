@@ -262,6 +262,13 @@ def read_traffic(op: str):
     return None, f"no ncu capture recorded for kernel-source hash {src}"
 
 
+def spin_ahead(torch):
+    """~1 ms of device spin ahead of a timed region: the host enqueues the region's launches
+    (and its closing event) before the GPU reaches them, so an event pair times the device
+    work only, not the host's launch overhead."""
+    torch.cuda._sleep(2_000_000)
+
+
 def instruction_ceiling(nv, torch, dev, iters=20000):
     """The NVFP4 MMA instruction ceiling measured now (nvfp4_debug_mma_rate): back-to-back
     tcgen05.mma kind::mxf4nvf4.block16 M256 N256 K64 on every SM pair; TFLOP/s = FLOPs of all
@@ -369,9 +376,13 @@ def run_ours(args, world, rank, local):
         nvml_index = torch.cuda._get_nvml_device_index(local)
     except Exception:
         nvml_index = local
-    # pass 1 (eager, an event before every launch): the per-kernel breakdown and the roofline
+    # pass 1 (eager, an event before every launch): the per-kernel breakdown and the roofline.
+    # A ~1 ms device spin ahead of each step lets the host enqueue the whole step before the
+    # GPU reaches it, so the launches run back to back (as in the graph replay) and each event
+    # difference is device time only, not host launch overhead.
     for k in range(K):
         flush()                    # evict L2 between steps (outside the timed events)
+        spin_ahead(torch)
         step(events[k])
     torch.cuda.synchronize()
     per_op = np.array([[events[k][i].elapsed_time(events[k][i + 1]) for i in range(len(ops))]
@@ -396,6 +407,7 @@ def run_ours(args, world, rank, local):
     with ClockSampler(nvml_index) as clocks:
         for k in range(K):
             flush()                    # evict L2 between steps (outside the timed events)
+            spin_ahead(torch)
             gev[k][0].record()
             graph.replay()
             gev[k][1].record()
@@ -437,6 +449,7 @@ def run_ours(args, world, rank, local):
         st_ms = []
         for it in range(max(args.warmup, 3) + K):
             flush()
+            spin_ahead(torch)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             nv.nvfp4_quantize(l.x, tensor_scale_in=ts_static, out=l.qa)
@@ -754,6 +767,7 @@ def run_sweep(args):
         for it in range(max(args.warmup, 3) + args.steps):
             for name, fn in (("quantize", l.quantize), ("gemm", l.gemm)):
                 flush()
+                spin_ahead(torch)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 fn()
@@ -812,6 +826,7 @@ def run_chain(args):
         ts = []
         for it in range(max(args.warmup, 3) + args.steps):
             flush()
+            spin_ahead(torch)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
             fn()
@@ -872,6 +887,7 @@ def run_fp8(args):
             for it in range(args.steps):
                 for name, fn in ops.items():
                     flush()
+                    spin_ahead(torch)
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record()
                     fn()
@@ -933,6 +949,7 @@ def run_attention(args):
         with sampler if name == "kernel" else _nullctx():
             for _ in range(args.steps):
                 flush()
+                spin_ahead(torch)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record()
                 fn()
@@ -977,6 +994,7 @@ def run_dit_block(args):
 
     def one(t):
         flush()
+        spin_ahead(torch)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         y = blk(x, timings=t)
@@ -999,6 +1017,7 @@ def run_dit_block(args):
     graph_ms = []
     for it in range(max(args.warmup, 3) + args.steps):
         flush()
+        spin_ahead(torch)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         replay()
