@@ -117,13 +117,14 @@ NVFP4_API size_t nvfp4_workspace_bytes(void);
  *   workspace  >= nvfp4_workspace_bytes() device bytes, 16-byte aligned, zero-filled
  *            before its first use and then reused (see nvfp4_workspace_bytes); may be NULL
  *            when tensor_scale_in is given.
- * Dynamic scale, x small enough to sit in the shared memory of all SMs (each CTA's rows
- * within 200 KB: M * K up to about 14.8M elements) and 16-byte aligned rows: one cooperative
- * launch reads x once into shared memory, reduces the amax, meets the other CTAs at a
- * grid-wide barrier on the workspace words and quantizes. Otherwise two launches: an amax
- * pass over x (skipped for a static scale), then the quantize pass, which walks x backwards
- * so that what the amax pass read last is still in L2. Codes and scales are identical
- * either way.
+ * Dynamic scale and 16-byte aligned rows, when at least a quarter of each CTA's rows fit in
+ * 200 KB of shared memory (one CTA per SM; M * K up to about 14.8M elements entirely, the
+ * down-projection input [4608, 12288] a quarter): one cooperative launch reads x, keeps
+ * those rows in shared memory, reduces the amax, meets the other CTAs at a grid-wide barrier
+ * on the workspace words and quantizes, reading only the rows not kept a second time.
+ * Otherwise two launches: an amax pass over x (skipped for a static scale), then the
+ * quantize pass, which walks x backwards so that what the amax pass read last is still in
+ * L2. Codes and scales are identical either way.
  * If a device-side wait of the single launch runs out of time (NVFP4_WAIT_TIMEOUT_NS,
  * default 2 s; it cannot under a cooperative launch unless the GPU misbehaves), tensor_scale
  * is written NaN, no codes are written, and the workspace must be zeroed before reuse.

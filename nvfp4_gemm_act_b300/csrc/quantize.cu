@@ -222,14 +222,16 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
 }
 
 // ---------------------------------------------------------------------------------------
-// Single-pass quantizer for activations that fit in the shared memory of the whole GPU (a
-// dynamic tensor scale only): one cooperative launch, one CTA per SM. CTA b loads rows
-// [b R, b R + R) of x into its shared memory -- all 1024 threads, 16-byte loads in batches of
+// Single-pass quantizer (a dynamic tensor scale only): one cooperative launch, one CTA per
+// SM. CTA b reads rows [b R, b R + R) of x -- all 1024 threads, 16-byte loads in batches of
 // six, so each SM keeps ~100 KB of x in flight (bulk copies from HBM keep far fewer bytes in
-// flight per SM) -- taking the amax from the registers on the way, and joins a grid-wide
-// barrier on workspace words (bounded spin; the cooperative launch guarantees every CTA is
-// resident). It then reads the tensor amax and quantizes its rows from shared memory: x is
-// read from HBM once, in one launch, instead of twice in two.
+// flight per SM) -- taking the amax from the registers on the way and keeping its first S
+// rows (S = R when they fit, else as many as 200 KB hold) in shared memory, and joins a
+// grid-wide barrier on workspace words (bounded spin; the cooperative launch guarantees every
+// CTA is resident). It then reads the tensor amax and quantizes its rows: the S resident rows
+// from shared memory, the others from global memory again, last-read first (the part of them
+// still in L2). When all rows are resident x is read from HBM once instead of twice; else
+// the S rows are not read twice, and the amax pass needs no launch of its own.
 //
 // Workspace words: ws[0] amax bits (atomic max), ws[1] CTAs arrived, ws[2] CTAs departed,
 // ws[3] failure flag. The CTA that departs last has seen every CTA pass the barrier and zeroes
@@ -238,16 +240,15 @@ __global__ void __launch_bounds__(kQuantThreads, 4)
 // ---------------------------------------------------------------------------------------
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedWarps = kFusedThreads / 32;
-constexpr int kFusedMaxRows = 64;               // rows per CTA
-constexpr int kFusedSmemData = 200 * 1024;      // bytes of x per CTA
+constexpr int kFusedSmemData = 200 * 1024;      // bytes of x per CTA held in shared memory
 constexpr int kFusedBatch = 6;                  // 16-byte loads in flight per thread
 
 __global__ void __launch_bounds__(kFusedThreads, 1)
     quantize_fused_kernel(const __nv_bfloat16* __restrict__ x, uint64_t ldx, uint32_t M, uint32_t Mpad,
-                          uint32_t K, uint32_t rows_per_cta, uint8_t* __restrict__ codes,
+                          uint32_t K, uint32_t rows_per_cta, uint32_t res_rows, uint8_t* __restrict__ codes,
                           uint8_t* __restrict__ scales, unsigned* ws, float* __restrict__ ts_out,
                           uint64_t timeout_ns) {
-  extern __shared__ __align__(128) uint8_t xs[];  // rows_per_cta rows of x, K * 2 bytes each
+  extern __shared__ __align__(128) uint8_t xs[];  // the first res_rows rows of x, K * 2 bytes each
   __shared__ float inv_tab[128];
   __shared__ uint32_t code_tab[128];
   __shared__ uint32_t warp_max[kFusedWarps];
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   // the rows are contiguous, so chunk c sits at byte 16 c
   const uint32_t vpr = K / 8u;
   const uint32_t nchunks = n_real * vpr;
+  const uint32_t res_chunks = min(n_real, res_rows) * vpr;  // chunks of the resident rows
   uint32_t m = 0u;
   for (uint32_t c0 = threadIdx.x; c0 < nchunks; c0 += kFusedBatch * kFusedThreads) {
     uint4 v[kFusedBatch];
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const uint32_t c = c0 + j * kFusedThreads;
       if (c < nchunks) {
         m = bf16x2_max_abs(m, bf16x2_max_abs(bf16x2_max_abs(v[j].x, v[j].y), bf16x2_max_abs(v[j].z, v[j].w)));
-        reinterpret_cast<uint4*>(xs)[c] = v[j];
+        if (c < res_chunks) reinterpret_cast<uint4*>(xs)[c] = v[j];
       }
     }
   }
@@ -316,8 +318,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if (threadIdx.x < 128) build_scale_table_entry(threadIdx.x, ts, inv_tab, code_tab);
     const ScaleRoute sr = scale_route(ts);
     __syncthreads();
-    // quantize: item = (row, 512-element chunk); lane = one 16-element block of the chunk;
-    // a warp takes two items at a time
+    // quantize: item = (row, 512-element chunk) -- last item first when some rows are read
+    // again (the rows read last are the ones most likely still in L2) --; lane = one
+    // 16-element block of the chunk; a warp takes two items at a time
     const uint32_t bpr = K / 16u, cpr = (bpr + 31u) / 32u, gpr = bpr >> 2;
     const uint32_t items = (r_end - r0) * cpr;
     const uint64_t row_code_bytes = (uint64_t)bpr * 8u;
@@ -327,17 +330,26 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       bool data[2], valid[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const uint32_t it = it0 + u * kFusedWarps;
+        const uint32_t idx = it0 + u * kFusedWarps;
+        const uint32_t it = idx < items ? (res_rows < r_end - r0 ? items - 1u - idx : idx) : 0u;
         const uint32_t i = it / cpr;
         bb[u] = (it - i * cpr) * 32u + lane;
         rr[u] = r0 + i;
-        valid[u] = it < items && bb[u] < bpr;
+        valid[u] = idx < items && bb[u] < bpr;
         data[u] = valid[u] && i < n_real;
         lo[u] = hi[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (data[u] && NVFP4_INDEX_OK(i * row_bytes + bb[u] * 32u + 32u <= rows_per_cta * row_bytes)) {
-          const uint4* src = reinterpret_cast<const uint4*>(xs + i * row_bytes + bb[u] * 32u);
-          lo[u] = src[0];
-          hi[u] = src[1];
+        if (data[u]) {
+          if (i < res_rows) {
+            if (NVFP4_INDEX_OK(i * row_bytes + bb[u] * 32u + 32u <= res_rows * row_bytes)) {
+              const uint4* src = reinterpret_cast<const uint4*>(xs + i * row_bytes + bb[u] * 32u);
+              lo[u] = src[0];
+              hi[u] = src[1];
+            }
+          } else if (NVFP4_INDEX_OK(rr[u] < M && bb[u] < bpr)) {
+            const __nv_bfloat16* g = x + (uint64_t)rr[u] * ldx + bb[u] * 16u;
+            lo[u] = ld_nc_v4(g);
+            hi[u] = ld_nc_v4(g + 8);
+          }
         }
       }
 #pragma unroll
@@ -567,10 +579,16 @@ cudaError_t launch_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
 
 namespace {
 
-// Rows per CTA of the single-pass quantizer for x [M, K] (0: x does not fit, or the copies
-// cannot be bulk copies).
-uint32_t fused_rows_per_cta(const void* x, int64_t M, int64_t K, int64_t ldx) {
-  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || (ldx * 2) % 16 != 0) return 0;
+// Rows per CTA of the single-pass quantizer for x [M, K] and how many of them stay in shared
+// memory ({0, 0}: x rows not 16-byte aligned, a row larger than the shared-memory budget, or
+// fewer than a quarter of each CTA's rows resident, where the two-pass path is the better one).
+struct FusedPlan {
+  uint32_t rows;
+  uint32_t res_rows;
+};
+
+FusedPlan fused_plan(const void* x, int64_t M, int64_t K, int64_t ldx) {
+  if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0 || (ldx * 2) % 16 != 0) return {0, 0};
   static const int per_sm = [] {
     int n = 0;
     if (cudaFuncSetAttribute(quantize_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -582,12 +600,13 @@ uint32_t fused_rows_per_cta(const void* x, int64_t M, int64_t K, int64_t ldx) {
     }
     return n;
   }();
-  if (per_sm < 1) return 0;
+  if (per_sm < 1) return {0, 0};
   const int64_t mpad = (M + 127) / 128 * 128;
   const int64_t ctas = static_cast<int64_t>(sm_count()) * per_sm;
   const int64_t rows = (mpad + ctas - 1) / ctas;
-  if (rows > kFusedMaxRows || rows * K * 2 > kFusedSmemData) return 0;
-  return static_cast<uint32_t>(rows);
+  const int64_t res = std::min<int64_t>(rows, kFusedSmemData / (K * 2));
+  if (res < 1 || res * 4 < rows) return {0, 0};
+  return {static_cast<uint32_t>(rows), static_cast<uint32_t>(res)};
 }
 
 }  // namespace
@@ -596,17 +615,18 @@ cudaError_t launch_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, ui
                             uint8_t* scales, unsigned* ws, const float* ts_in, float* ts_out,
                             cudaStream_t s) {
   if (ts_in == nullptr && M > 0) {
-    if (const uint32_t rows = fused_rows_per_cta(x, M, K, ldx); rows != 0) {
+    if (const FusedPlan plan = fused_plan(x, M, K, ldx); plan.rows != 0) {
       const int64_t mpad = (M + 127) / 128 * 128;
-      const unsigned grid = static_cast<unsigned>((mpad + rows - 1) / rows);
+      const unsigned grid = static_cast<unsigned>((mpad + plan.rows - 1) / plan.rows);
       const __nv_bfloat16* xp = static_cast<const __nv_bfloat16*>(x);
       uint64_t ld = static_cast<uint64_t>(ldx);
       uint32_t m = static_cast<uint32_t>(M), mp = static_cast<uint32_t>(mpad), k = static_cast<uint32_t>(K);
-      uint32_t r = rows;
+      uint32_t r = plan.rows, rr = plan.res_rows;
       uint64_t limit = wait_timeout_ns();
-      void* args[] = {&xp, &ld, &m, &mp, &k, &r, &codes, &scales, &ws, &ts_out, &limit};
+      void* args[] = {&xp, &ld, &m, &mp, &k, &r, &rr, &codes, &scales, &ws, &ts_out, &limit};
       return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(quantize_fused_kernel), dim3(grid),
-                                         dim3(kFusedThreads), args, static_cast<size_t>(rows) * K * 2, s);
+                                         dim3(kFusedThreads), args, static_cast<size_t>(plan.res_rows) * K * 2,
+                                         s);
     }
   }
   if (ts_in == nullptr) {

@@ -215,9 +215,10 @@ def test_scale_rounding_boundaries_dynamic_scale(k):
 
 
 def test_large_ragged_strided_dynamic_scale():
-    # X of 1300 x 12288 (32 MB: too large for the SMs' shared memory, so the amax and quantize
-    # passes run as two launches); ragged M (108 padding rows of scale tiles, which must come
-    # out zero from an uninitialised buffer) and a row pitch of 12352 elements
+    # X of 1300 x 12288 (32 MB: too large for the SMs' shared memory, so the single-pass
+    # launch keeps 8 of each CTA's 10 rows there and reads the other 2 again after the grid
+    # barrier); ragged M (108 padding rows of scale tiles, which must come out zero from an
+    # uninitialised buffer) and a row pitch of 12352 elements
     w = W.DOWN_BIAS.with_m(1300, seed=91)
     x = W.make_x(w)
     big = torch.zeros(1300, 12288 + 64, dtype=torch.bfloat16)
@@ -236,3 +237,29 @@ def test_large_ragged_strided_dynamic_scale():
     r, kb = np.meshgrid(np.arange(1300), np.arange(12288 // 16), indexing="ij")
     used[R.scale_offset(r, kb, 12288)] = True
     assert not buf[~used].any(), "padding rows of the scale tiles must be zero"
+
+
+def test_dynamic_scale_rows_larger_than_shared_memory():
+    # a row of 106,496 elements (208 KB) does not fit the single-pass kernel's shared memory at
+    # all: the amax pass and the quantize pass run as two launches; ragged M
+    K = 106496
+    x = _bf16(np.random.default_rng(94).standard_normal((70, K)) * 0.5)
+    q = nv.nvfp4_quantize(x.to(DEV))
+    assert_quant_equal(gpu_nvfp4_to_np(q), R.quantize_ref(to_np_f32(x)), "two-pass dynamic")
+
+
+@pytest.mark.parametrize("M,K", [(4608, 6144), (2000, 12288), (150, 24576)])
+def test_dynamic_scale_partly_resident_rows(M, K):
+    # single-pass launches where only some of each CTA's rows stay in shared memory (X
+    # [4608, 6144]: 16 of 32; [2000, 12288]: 8 of 14; [150, 24576]: both of 2): the resident
+    # rows and the re-read rows quantize alike, bit for bit, on sampled rows
+    x = _bf16(0.5 * np.random.default_rng(95 + M).standard_t(3, (M, K)))
+    q = nv.nvfp4_quantize(x.to(DEV))
+    gc, gs, gt = gpu_nvfp4_to_np(q)
+    xn = to_np_f32(x)
+    ts = R.tensor_scale_ref(xn)
+    rows = np.unique(np.concatenate([[0, 1, 7, 8, 9, 13, 14, 15, 16, 31, 32, M - 1],
+                                     np.random.default_rng(96).integers(0, M, 40)]))
+    rows = rows[rows < M]
+    rc, rs, _ = R.quantize_ref(xn[rows], ts)
+    assert_quant_equal((gc[rows], gs[rows], gt), (rc, rs, ts), f"partly resident {M}x{K}")
