@@ -20,11 +20,14 @@ def _bf16(shape, seed, scale=1.0):
 def _run_all():
     """Every instrumented call on ragged shapes; returns the outputs, in a fixed order."""
     outs = []
-    # activation quantizer: single-pass (dynamic), two-pass (dynamic), static with a row stride
+    # activation quantizer: single pass with all rows in shared memory, single pass with part
+    # of them there (dynamic), two passes (dynamic), static with a row stride
     x1 = _bf16((200, 320), 1)
     outs += list(nv.nvfp4_quantize(x1)[:3])
-    x2 = _bf16((2000, 8192), 2, 3.0)  # too large for the single-pass kernel
+    x2 = _bf16((2000, 8192), 2, 3.0)  # 12 of each CTA's 14 rows kept in shared memory
     outs += list(nv.nvfp4_quantize(x2)[:3])
+    x4 = _bf16((70, 106496), 5)  # a row larger than the shared-memory budget: two passes
+    outs += list(nv.nvfp4_quantize(x4)[:3])
     x3 = _bf16((200, 328), 3)[:, :320]
     outs += list(nv.nvfp4_quantize(x3, tensor_scale_in=torch.tensor([0.01], device=DEV))[:3])
     # weight packer, plain and gated; GEMMs with every epilogue and output format
