@@ -65,11 +65,13 @@ def test_noalloc_matches_workspace_quantizer_on_two_calls():
 
 
 @pytest.mark.gpu
-def test_noalloc_two_launch_path_matches_on_two_calls():
-    # 4608 x 12288 is too large for the single cooperative launch: the amax pass and the
-    # quantize pass run as two kernels on the library's scratch words
+@pytest.mark.parametrize("shape", [(4608, 12288), (300, 106496)])
+def test_noalloc_large_inputs_match_on_two_calls(shape):
+    # 4608 x 12288 is too large for the SMs' shared memory: the single cooperative launch keeps
+    # a quarter of its rows there and reads the rest twice. A row of 106,496 elements (208 KB)
+    # does not fit at all: the amax pass and the quantize pass run as two kernels. Both use the
+    # library's scratch words.
     rng = np.random.default_rng(4321)
-    shape = (4608, 12288)
     x1 = torch.from_numpy((rng.standard_t(3, size=shape) * 4.0).astype(np.float32)).to(torch.bfloat16).cuda()
     x2 = torch.from_numpy((rng.standard_t(3, size=shape) * 0.5).astype(np.float32)).to(torch.bfloat16).cuda()
     ts_seen = []
