@@ -303,8 +303,14 @@ __device__ __forceinline__ void epilogue_row(const EpiParams& p, const QuantOut&
     for (int c = 0; c < 4; ++c) {
       if (c0 + c * 32 < p.norm_cols) {
         const float scale = rsqrtf(fmaf(hs[c], inv_hd, p.eps));
+        // (z * scale) * gamma, two columns per packed multiply: the same roundings as scalar
+        const uint64_t sc2 = f32x2(scale, scale);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) z[c * 32 + i] = z[c * 32 + i] * scale * gamma_s[c * 32 + i];
+        for (int i = 0; i < 32; i += 2) {
+          const float2 g = *reinterpret_cast<const float2*>(gamma_s + c * 32 + i);
+          const uint64_t t = mul_f32x2(f32x2(z[c * 32 + i], z[c * 32 + i + 1]), sc2);
+          unpack_f32x2(mul_f32x2(t, f32x2(g.x, g.y)), z[c * 32 + i], z[c * 32 + i + 1]);
+        }
       }
     }
   }
@@ -596,8 +602,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tm_a, const CUtenso
       for (int w = 0; w < kEpiWarps; ++w) all_ready = all_ready && tile_flags[w] != 0;
       if (!all_ready) break;  // uniform across the epilogue warps
       const float* bh = bias_s + half * kHalf;
+      {  // z = alpha * acc + bias, two columns per packed FMA (each half rounded as fmaf)
+        const uint64_t a2 = f32x2(alpha, alpha);
 #pragma unroll
-      for (int i = 0; i < kHalf; ++i) z[i] = fmaf(alpha, z[i], bh[i]);
+        for (int i = 0; i < kHalf; i += 2) {
+          const float2 b = *reinterpret_cast<const float2*>(bh + i);
+          unpack_f32x2(fma_f32x2(a2, f32x2(z[i], z[i + 1]), f32x2(b.x, b.y)), z[i], z[i + 1]);
+        }
+      }
       epilogue_row(ep, qo, &tm_out, z, m_blk * kBM + q * 32, n_base + half * kHalf, half, row_local,
                    gamma_s + half * kHalf, xch, sbase + kOffEpiBuf + ew * kEpiBufBytes, lane);
     }
