@@ -212,33 +212,47 @@ __device__ __forceinline__ void store_rows(const EpiParams& p, const void* tm_ou
 }
 
 // NVFP4 output of this thread's row (row0 + lane): its NV values y[] are output columns
-// [col0, col0 + NV) (col0 a multiple of 16, NV of 64). Each 16-value block is rounded to bf16
-// and quantized; rows past M (padding of the 128-row scale tiles) get zero scales.
+// [col0, col0 + NV) (col0 and NV multiples of 64). Each 16-value block is rounded to bf16 and
+// quantized; rows past M (padding of the 128-row scale tiles) get zero scales. Codes leave in
+// 16-byte stores, a group's four scale bytes in one 32-bit store.
 template <int NV>
 __device__ __forceinline__ void store_rows_nvfp4(const EpiParams& p, const QuantOut& qo, const float* y, int row0,
                                                  int col0, int width, int lane) {
+  static_assert(NV % 64 == 0, "whole 64-column groups");
   const int row = row0 + lane;
   const uint32_t gpr = static_cast<uint32_t>(width) >> 6;  // 64-column scale atoms per row band
   const bool real = row < p.M;
+  // a group of 4 blocks (64 columns, col a multiple of 64 and width % 64 == 0, so a group lies
+  // wholly inside or wholly past the width): 32 code bytes contiguous in the row, 4 scale
+  // bytes contiguous in the tiled layout (blocks 4g..4g+3 of one row)
 #pragma unroll
-  for (int b = 0; b < NV / 16; ++b) {
-    const int col = col0 + b * 16;
+  for (int g = 0; g < NV / 64; ++g) {
+    const int col = col0 + g * 64;
     if (col >= width) break;
-    const float* v = y + b * 16;
-    const uint4 lo = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                pack_bf16x2(v[6], v[7]));
-    const uint4 hi = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
-                                pack_bf16x2(v[14], v[15]));
-    uint32_t stored = 0u;
-    if (real) {
-      uint2 c;
-      stored = quantize_block(lo, hi, qo.sr, qo.inv_tab, qo.code_tab, c);
-      if (NVFP4_INDEX_OK(row >= 0 && col >= 0 && (col & 15) == 0 && col + 16 <= width))
-        *reinterpret_cast<uint2*>(p.out_codes + (int64_t)row * (width >> 1) + (col >> 1)) = c;
+    uint32_t w[8];
+    uint32_t sc = 0u;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float* v = y + g * 64 + b * 16;
+      const uint4 lo = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                  pack_bf16x2(v[6], v[7]));
+      const uint4 hi = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                                  pack_bf16x2(v[14], v[15]));
+      uint2 c = make_uint2(0u, 0u);
+      const uint32_t stored = real ? quantize_block(lo, hi, qo.sr, qo.inv_tab, qo.code_tab, c) : 0u;
+      w[2 * b] = c.x;
+      w[2 * b + 1] = c.y;
+      sc |= stored << (8 * b);
+    }
+    if (real && NVFP4_INDEX_OK(row >= 0 && col >= 0 && (col & 63) == 0 && col + 64 <= width)) {
+      uint4* dst = reinterpret_cast<uint4*>(p.out_codes + (int64_t)row * (width >> 1) + (col >> 1));
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     }
     const uint32_t soff = scale_offset(static_cast<uint32_t>(row), static_cast<uint32_t>(col >> 4), gpr);
-    if (NVFP4_INDEX_OK(row >= 0 && static_cast<int64_t>(soff) < static_cast<int64_t>((p.M + 127) / 128) * gpr * 512))
-      p.out_scales[soff] = static_cast<uint8_t>(stored);
+    if (NVFP4_INDEX_OK(row >= 0 && (soff & 3u) == 0u &&
+                       static_cast<int64_t>(soff) + 4 <= static_cast<int64_t>((p.M + 127) / 128) * gpr * 512))
+      *reinterpret_cast<uint32_t*>(p.out_scales + soff) = sc;
   }
 }
 
