@@ -219,6 +219,9 @@ template <int NV>
 __device__ __forceinline__ void store_rows_nvfp4(const EpiParams& p, const QuantOut& qo, const float* y, int row0,
                                                  int col0, int width, int lane) {
   static_assert(NV % 64 == 0, "whole 64-column groups");
+  // rows past the scale tiles' padding (the second CTA of the last row pair when M spans an
+  // odd number of 128-row blocks) have neither codes nor scales (uniform across the warp)
+  if (row0 >= ((p.M + 127) / 128) * 128) return;
   const int row = row0 + lane;
   const uint32_t gpr = static_cast<uint32_t>(width) >> 6;  // 64-column scale atoms per row band
   const bool real = row < p.M;

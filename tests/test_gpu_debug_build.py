@@ -43,10 +43,14 @@ def _run_all():
         for od in (torch.bfloat16, torch.float32):
             outs.append(nv.nvfp4_gemm(qa, qb, epi, out_dtype=od, **kw))
     w2 = _bf16((320, 256), 5, 0.02)
+    # NVFP4 outputs for 200 rows (two 128-row blocks) and 300 rows (three: the last row pair's
+    # second CTA lies wholly past the padded rows and must store nothing)
+    qa3 = nv.nvfp4_quantize(_bf16((300, 320), 8))
     for gated, epi in ((False, "bias"), (True, "gated_silu")):
         qb = nv.nvfp4_pack_weights(w2, gated_interleave=gated)
-        q = nv.nvfp4_gemm_nvfp4_out(qa, qb, epi, torch.tensor([0.002], device=DEV))
-        outs += [q.codes, q.scales]
+        for a_op in (qa, qa3):
+            q = nv.nvfp4_gemm_nvfp4_out(a_op, qb, epi, torch.tensor([0.002], device=DEV))
+            outs += [q.codes, q.scales]
     # FP8 variant
     fa = nv.fp8_quantize(x1)
     fb = nv.fp8_pack_weights(w, gated_interleave=True)
