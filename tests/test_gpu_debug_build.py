@@ -51,6 +51,8 @@ def _run_all():
         for a_op in (qa, qa3):
             q = nv.nvfp4_gemm_nvfp4_out(a_op, qb, epi, torch.tensor([0.002], device=DEV))
             outs += [q.codes, q.scales]
+    # a bf16 GEMM over the same three row blocks
+    outs.append(nv.nvfp4_gemm(qa3, nv.nvfp4_pack_weights(w, gated_interleave=False), "bias", bias=bias))
     # FP8 variant
     fa = nv.fp8_quantize(x1)
     fb = nv.fp8_pack_weights(w, gated_interleave=True)
