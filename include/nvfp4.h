@@ -182,9 +182,11 @@ NVFP4_API nvfp4_status nvfp4_pack_weights(const void *w, int64_t K, int64_t N, i
  *          for BF16, % 4 for FP32).
  *   device_error  optional int [1]: receives NVFP4_ERR_TIMEOUT if a device wait runs out;
  *          the caller zeroes it. NULL: device timeouts are not reported.
- * Rules: M >= 0, N > 0, N % 32 == 0, K > 0, K % 64 == 0, all code and scale pointers
- * 16-byte aligned. M == 0 launches nothing and returns NVFP4_OK after the shape and enum
- * checks (the pointers may then be NULL).
+ * Rules: M >= 0, N > 0, N % 32 == 0, K > 0, K % 64 == 0, M * K < 2^34 and N * K < 2^34 (the
+ * operand bounds of nvfp4_quantize and nvfp4_pack_weights), ceil(M / 256) * ceil(N / 256) <
+ * 2^31 (256 x 256 output tiles), all code and scale pointers 16-byte aligned. Shapes outside
+ * these return NVFP4_ERR_SHAPE. M == 0 launches nothing and returns NVFP4_OK after the shape
+ * and enum checks (the pointers may then be NULL).
  */
 NVFP4_API nvfp4_status nvfp4_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const float *a_ts,
                         const uint8_t *b_codes, const uint8_t *b_scales, const float *b_ts,

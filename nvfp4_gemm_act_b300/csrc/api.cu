@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdint>
 #include <cstdlib>
 #include <initializer_list>
 #include <mutex>
@@ -200,6 +201,10 @@ nvfp4_status gemm_args(const uint8_t* a_codes, const uint8_t* a_scales, const fl
   }
   if (M < 0 || N <= 0 || N % 32 != 0 || K <= 0 || K % 64 != 0) return NVFP4_ERR_SHAPE;
   if (M > (int64_t(1) << 31) - 1 || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return NVFP4_ERR_SHAPE;
+  // operands no larger than the quantizer and packer produce (M * K and N * K below 2^34), and
+  // the kernel's pair-tile index and row coordinates within 32 bits
+  if ((M > 0 && K > kMaxElems / M) || K > kMaxElems / N) return NVFP4_ERR_SHAPE;
+  if (((M + 255) / 256) * ((N + 255) / 256) > int64_t{INT32_MAX}) return NVFP4_ERR_SHAPE;
   if (epi == NVFP4_EPI_HEAD_RMSNORM && (norm_cols < 0 || norm_cols > N || norm_cols % head_dim != 0))
     return NVFP4_ERR_SHAPE;
   out_cols = epi == NVFP4_EPI_GATED_SILU ? N / 2 : N;

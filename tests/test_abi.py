@@ -111,6 +111,12 @@ def test_gemm_host_checks():
     assert g(od=1, ldo=260) == ERR_SHAPE or g(od=1, ldo=260) != ERR_ALIGN
     assert g(M=0) == OK
     assert g(M=0, ac=None) == OK
+    # operands larger than the quantizer / packer can produce, and more pair tiles than a
+    # 32-bit index holds: refused before any device work
+    assert g(M=2**31 - 1, N=256, K=64, ldo=256) == ERR_SHAPE     # M * K >= 2^34
+    assert g(N=2**30, K=2**14, ldo=2**30) == ERR_SHAPE            # N * K >= 2^34
+    assert g(M=2**25, N=2**25, K=64, ldo=2**25) == ERR_SHAPE      # 2^34 pair tiles
+    assert g(M=2**20, N=2**20, K=64, ldo=2**20) != ERR_SHAPE      # within every bound
 
 
 def gq(**kw):
